@@ -1,0 +1,105 @@
+"""Seeded synthetic inputs for the KDA forward.
+
+This module only draws random numbers; it holds none of the method's
+arithmetic.  Both the CUDA path's tests/benchmark and the fp64 oracle consume
+the tensors it returns, so the two sides see identical bits.
+
+Distributions follow the workloads of the KDA forward kernels (kernel-fun
+``kda/_kernels/fwd_state.py`` host wrapper: bf16 q/k/v, fp32 per-dimension
+log-decay g, fp32 initial/final state) and the standard KDA setup:
+
+* q, k: N(0,1) in fp32, L2-normalised over K per token, then rounded to bf16;
+* v: N(0,1) rounded to bf16;
+* beta: sigmoid(N(0,1)) rounded to bf16, shape [B,T,H] (already activated);
+* g: logsigmoid(N(mu,1)) in fp32, shape [B,T,H,K] (natural-log decay, < 0);
+* h0: 0.1 * N(0,1) fp32 [N,H,K,V], or None (zero initial state);
+* scale = K ** -0.5.
+
+Generation runs on the CPU with ``torch.Generator`` (seed per workload) so the
+bits do not depend on the device.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+import torch.nn.functional as F
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    K: int
+    V: int
+    mu: float = 3.0
+    h0: bool = True
+    varlen: int = 0          # number of packed sequences (0 = fixed length)
+    max_len: int = 8192      # varlen lengths are uniform in [1, max_len]
+    seed: int = 20261202
+    note: str = field(default="", compare=False)
+
+
+# The five workloads of the KDA forward: a tiny two-chunk case the oracle
+# finishes instantly, a mid-size case, the headline shape, a packed varlen
+# batch and a single long sequence (few scan CTAs, long serial chain).
+WORKLOADS = {
+    "tiny": Workload("tiny", B=1, T=128, H=1, K=64, V=64, h0=False, seed=20261202),
+    "mid": Workload("mid", B=1, T=4096, H=16, K=128, V=128, seed=20261203),
+    "headline": Workload("headline", B=4, T=8192, H=32, K=128, V=128, seed=20261204),
+    "varlen": Workload("varlen", B=1, T=0, H=32, K=128, V=128, varlen=16, seed=20261205),
+    "long": Workload("long", B=1, T=65536, H=32, K=128, V=128, mu=5.0, h0=False,
+                     seed=20261206),
+}
+
+
+def varlen_lengths(n: int, max_len: int, seed: int) -> list[int]:
+    """n sequence lengths uniform in [1, max_len] (seeded)."""
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randint(1, max_len + 1, (n,), generator=gen).tolist()
+
+
+def cu_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def make_inputs(w: Workload, lengths=None, h0=None, dtype_g=torch.float32):
+    """Draw the inputs of workload ``w`` on the CPU.
+
+    Returns a dict with q, k, v (bf16 [B,T,H,K|V]), g (fp32 [B,T,H,K]), beta
+    (bf16 [B,T,H]), h0 (fp32 [N,H,K,V] or None), cu_seqlens (int32 [N+1] or
+    None), scale (float), N, and the shape fields.
+    """
+    gen = torch.Generator().manual_seed(w.seed)
+    if w.varlen:
+        if lengths is None:
+            lengths = varlen_lengths(w.varlen, w.max_len, w.seed + 7919)
+        cu = cu_from_lengths(lengths)
+        B, T, N = 1, int(cu[-1]), len(lengths)
+    elif lengths is not None:
+        cu = cu_from_lengths(lengths)
+        B, T, N = 1, int(cu[-1]), len(lengths)
+    else:
+        cu = None
+        B, T, N = w.B, w.T, w.B
+    H, K, V = w.H, w.K, w.V
+
+    def unit_rows(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        return x.to(torch.bfloat16)
+
+    q = unit_rows((B, T, H, K))
+    k = unit_rows((B, T, H, K))
+    v = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen)).to(torch.bfloat16)
+    g = F.logsigmoid(torch.randn((B, T, H, K), generator=gen) + w.mu).to(dtype_g)
+    if h0 is None and w.h0:
+        h0 = 0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=K ** -0.5,
+                B=B, T=T, H=H, K=K, V=V, N=N)

@@ -1,0 +1,131 @@
+"""Chunked KDA forward in fp64 numpy -- TEST INFRASTRUCTURE (see oracle/__init__).
+
+This is the chunkwise algorithm that the GPU path implements, written step by
+step in the notation of kernel-fun ``kda/_kernels/fwd_state.py`` (module
+docstring: the intra-stage operands ``qg``, ``kg``, ``Aqk``, ``w``, ``u``, the
+per-chunk decay vector ``G`` = last row of ``g2``, and the per-chunk scan
+``WH = w@h; v' = u - WH; o = scale*qg@h + Aqk@v'; h <- exp2(G)*h + kg^T@v'``).
+The two operands that fwd_state.py consumes but does not define, ``w`` and
+``u``, follow from the per-token recurrence: with the inclusive in-chunk decay
+gamma_i = exp2(g2_i),
+
+    A[i, j] = beta_i * sum_d k_id k_jd exp2(g2_id - g2_jd)      (j < i, else 0)
+    T       = (I + A)^-1                                          (unit lower triangular)
+    w       = T diag(beta) (k * exp2(g2)),   u = T diag(beta) v
+
+so that v' = u - w @ h is the chunk's vector of delta-rule corrections.
+FlashKDA (the "KDA源码剖析之FlashKDA（下）" walk-through, its INV operand) uses the
+same inverse at chunk 16.
+
+No blocking or reassociation is done beyond what these equations state: every
+gate factor is an explicit exp2 of a difference, so nothing overflows for any
+finite decay.  A tail chunk (sequence length not a multiple of C) is padded
+with inert rows (q = k = v = 0, g = 0, beta = 0), which leaves the recurrence
+over the valid rows unchanged.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+LOG2E = 1.0 / np.log(2.0)
+
+
+def _pad_rows(x, C):
+    n = x.shape[0]
+    r = (-n) % C
+    if r == 0:
+        return x
+    pad = np.zeros((r,) + x.shape[1:], dtype=x.dtype)
+    return np.concatenate([x, pad], axis=0)
+
+
+def chunk_intra(q, k, v, g, beta, scale, C=64):
+    """Intra-chunk stage for one (sequence, head).
+
+    q, k, g: [L, K]; v: [L, V]; beta: [L] (fp64).  Returns a list (one entry per
+    chunk) of dicts with keys ``g2`` [C,K] (log2-space inclusive cumsum),
+    ``G`` [K], ``qg``, ``kg`` [C,K], ``Aqk`` [C,C] (scale folded in, zero above
+    the diagonal), ``A`` [C,C] (strictly lower), ``T`` [C,C], ``w`` [C,K],
+    ``u`` [C,V], ``valid`` (number of real rows).
+    """
+    L = q.shape[0]
+    q, k, v, g = (_pad_rows(np.asarray(x, np.float64), C) for x in (q, k, v, g))
+    beta = _pad_rows(np.asarray(beta, np.float64), C)
+    out = []
+    for c0 in range(0, q.shape[0], C):
+        sl = slice(c0, c0 + C)
+        qc, kc, vc, gc, bc = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        g2 = np.cumsum(gc, axis=0) * LOG2E           # chunk-local cumsum / ln2
+        G = g2[-1].copy()                            # padded rows carry g = 0
+        lower_eq = np.tril(np.ones((C, C), dtype=bool))       # j <= i
+        lower = np.tril(np.ones((C, C), dtype=bool), k=-1)    # j < i
+        # gate[i, j, d] = exp2(g2_id - g2_jd), only where it is used (j <= i)
+        diff = g2[:, None, :] - g2[None, :, :]
+        diff = np.where(lower_eq[:, :, None], diff, -np.inf)
+        gate = np.exp2(diff)
+        Aqk = scale * np.einsum("id,jd,ijd->ij", qc, kc, gate)
+        Akk = np.einsum("id,jd,ijd->ij", kc, kc, gate)
+        A = np.where(lower, bc[:, None] * Akk, 0.0)
+        T = np.linalg.inv(np.eye(C) + A)
+        w = T @ (bc[:, None] * (kc * np.exp2(g2)))
+        u = T @ (bc[:, None] * vc)
+        qg = qc * np.exp2(g2)
+        kg = kc * np.exp2(G[None, :] - g2)
+        out.append(dict(g2=g2, G=G, qg=qg, kg=kg, Aqk=Aqk, A=A, T=T, w=w, u=u,
+                        valid=min(C, L - c0)))
+    return out
+
+
+def chunk_scan(chunks, h0, scale):
+    """Inter-chunk state scan for one (sequence, head).
+
+    ``chunks`` from :func:`chunk_intra`; h0 [K, V].  Returns (o [L, V], ht [K, V]).
+    """
+    h = np.array(h0, dtype=np.float64, copy=True)
+    outs = []
+    for ch in chunks:
+        WH = ch["w"] @ h
+        vp = ch["u"] - WH
+        o = scale * (ch["qg"] @ h) + ch["Aqk"] @ vp
+        h = np.exp2(ch["G"])[:, None] * h + ch["kg"].T @ vp
+        outs.append(o[: ch["valid"]])
+    V = h.shape[1]
+    o = np.concatenate(outs, axis=0) if outs else np.zeros((0, V))
+    return o, h
+
+
+def chunked_fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, C=64):
+    """Chunked KDA forward over all sequences and heads, fp64.
+
+    Same shapes and sequence conventions as :func:`oracle.recurrent_fwd`; the
+    inputs are numpy arrays already in float64 (or anything numpy converts).
+    Returns (o [B,T,H,V], ht [N,H,K,V]).
+    """
+    q, k, v, g, beta = (np.asarray(x, np.float64) for x in (q, k, v, g, beta))
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is None:
+        cu = np.arange(B + 1) * T
+        N = B
+        flat = lambda x: x.reshape((B * T,) + x.shape[2:])  # noqa: E731
+    else:
+        assert B == 1
+        cu = np.asarray(cu_seqlens, np.int64)
+        N = len(cu) - 1
+        flat = lambda x: x[0]  # noqa: E731
+    qf, kf, vf, gf, bf = (flat(x) for x in (q, k, v, g, beta))
+    o = np.zeros((B * T, H, V))
+    ht = np.zeros((N, H, K, V))
+    for s in range(N):
+        a, b = int(cu[s]), int(cu[s + 1])
+        for h in range(H):
+            h0sh = np.zeros((K, V)) if h0 is None else np.asarray(h0, np.float64)[s, h]
+            if b == a:
+                ht[s, h] = h0sh
+                continue
+            chunks = chunk_intra(qf[a:b, h], kf[a:b, h], vf[a:b, h], gf[a:b, h], bf[a:b, h],
+                                 scale, C)
+            os_, hs = chunk_scan(chunks, h0sh, scale)
+            o[a:b, h] = os_
+            ht[s, h] = hs
+    return o.reshape(B, T, H, V), ht
