@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 KDA chunked forward; prints one JSON line.
+
+A step is one full forward (chunk planner + intra-chunk kernel + scan kernel)
+over the headline workload (B=4, H=32, T=8192, K=V=128, bf16 I/O, fp32
+state), inputs resident in HBM.  The inputs (1.6 GB) are larger than L2, so
+no flush is done between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores.  Under
+torchrun each rank runs an independent replica (the path shards into
+independent (sequence, head) units; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd tokens/s (B=4,H=32,T=8192,K=V=128 bf16); % of HBM/TC roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def bytes_per_token_head(K, V, C=64):
+    """Algorithmic HBM bytes per token-head of each kernel (two-stage chunked form)."""
+    intra = (2 * K * 2 + V * 2 + K * 4 + 2) + (3 * K * 2 + V * 2 + C * 2 + K * 4 / C)
+    scan = (3 * K * 2 + C * 2 + V * 2 + K * 4 / C) + V * 2
+    return intra, scan
+
+
+def flops_per_token_head(K, V, C=64):
+    """Chunked-form flops per token-head (Aqk, A, w, u; WH, qg@h, kg^T v'; Aqk@v')."""
+    per_chunk = 4 * 2 * C * C * K / 2 + 0 * 0  # Aqk/A (2 C^2 K each) + w (2 C^2 K) + u (2 C^2 V)
+    per_chunk = 2 * C * C * K * 3 + 2 * C * C * V + 3 * 2 * C * K * V + 2 * C * C * V
+    return per_chunk / C
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_name, src_file, workload):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the
+    kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha(src_file)
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if (kv.get("kernel") == kernel_name and kv.get("workload") == workload
+                    and kv.get("source_sha") == sha):
+                try:
+                    return float(kv["dram_bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(x, seconds, cores):
+    """Time the fp64 oracle on a bounded sample of (sequence, head) units of the
+    workload; returns (tokens/s scaled to whole tokens, description, threads)."""
+    import numpy as np
+    import oracle
+    B, T, H = x["B"], x["T"], x["H"]
+    # calibrate with one unit on one thread
+    sub = lambda nh: {n: x[n][:1, :, :nh].contiguous() for n in ("q", "k", "v", "g", "beta")}  # noqa: E731
+    one = sub(1)
+    h0 = None if x["h0"] is None else x["h0"][:1, :1].contiguous()
+    t0 = time.perf_counter()
+    oracle.recurrent_fwd(one["q"], one["k"], one["v"], one["g"], one["beta"], x["scale"], h0=h0,
+                         nthreads=1)
+    t1 = time.perf_counter() - t0
+    nh = int(max(1, min(H, round(seconds * cores / max(t1, 1e-6)))))
+    s = sub(nh)
+    h0 = None if x["h0"] is None else x["h0"][:1, :nh].contiguous()
+    th = min(cores, nh)
+    t0 = time.perf_counter()
+    oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], x["scale"], h0=h0, nthreads=th)
+    dt = time.perf_counter() - t0
+    tokens_equiv = T * nh / H
+    desc = (f"fp64 oracle on {nh} of the {B * H} (sequence, head) units (sequence 0, heads 0..{nh - 1}), "
+            f"{T} tokens each; rate scaled to whole {H}-head tokens")
+    return tokens_equiv / dt, desc, th, dt
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    from chunked_gated_delta_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    cores = host_cores()
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, desc, th, dt = oracle_sample_rate(x, args.ref_seconds, cores)
+        if i >= args.warmup:
+            rates.append((r, dt))
+    value = statistics.median(r for r, _ in rates)
+    ms = statistics.median(dt for _, dt in rates) * 1000
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": workload_config(w, x),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, x):
+    return {"workload": f"{w.name}: B={x['B']} H={x['H']} T={x['T']} K={x['K']} V={x['V']} chunk=64",
+            "B": x["B"], "T": x["T"], "H": x["H"], "K": x["K"], "V": x["V"], "chunk": 64,
+            "l2": "inputs (~1.6 GB) larger than L2 (129 MB); no flush between steps",
+            "parallelism": "independent replica per GPU"}
+
+
+def run_gb300(args):
+    import torch
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    import chunked_gated_delta_gb300 as kda
+    from chunked_gated_delta_gb300 import synth
+    kda.load_library(build_if_missing=True)
+
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    B, T, H, K, V, N = x["B"], x["T"], x["H"], x["K"], x["V"], x["N"]
+    d = {n: (x[n].to(dev) if isinstance(x[n], torch.Tensor) else x[n]) for n in x}
+    dims = kda.make_dims(B, T, H, K, V, 0 if x["cu_seqlens"] is None else N)
+    ws = kda.new_workspace(dims, dev)
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_mid=None):
+        kda.fwd_intra(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dims, ws, stream)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        kda.fwd_scan(d["scale"], d["h0"], o, ht, dims, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = kda.status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"kernel status {st}")
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0[0].record(stream)
+    for i in range(args.steps):
+        step(ev1[i])
+        ev0[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = ev0[0].elapsed_time(ev0[-1])
+    intra_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    scan_ms = [ev1[i].elapsed_time(ev0[i + 1]) for i in range(args.steps)]
+    ms_per_step = max_over_ranks(total_ms / args.steps, world)
+    tokens = B * T
+    value = tokens * world / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel
+    hbm, tc, tc_sus, peak_kind = peaks()
+    b_intra, b_scan = bytes_per_token_head(K, V)
+    th = tokens * H
+    hstate = 2 * N * H * K * V * 4 if x["h0"] is not None else N * H * K * V * 4
+    intra_avg = statistics.mean(intra_ms)
+    scan_avg = statistics.mean(scan_ms)
+    if scan_avg >= intra_avg:
+        dom, dom_ms, dom_bytes, src = "kda_scan_kernel", scan_avg, b_scan * th + hstate, "scan.cu"
+    else:
+        dom, dom_ms, dom_bytes, src = "kda_intra_kernel", intra_avg, b_intra * th, "intra.cu"
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    traffic = ncu_traffic(dom, os.path.join(ROOT, "chunked_gated_delta_gb300", "csrc", src), w.name)
+    step_bytes = (b_intra + b_scan) * th + hstate
+    step_flops = flops_per_token_head(K, V) * th
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the KDA forward workloads)",
+        "config": workload_config(w, x),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms},
+        "step_roofline": {"bytes": step_bytes, "hbm_ms": step_bytes / (hbm * 1e9) * 1e3,
+                          "flops": step_flops, "tc_ms": step_flops / (tc * 1e12) * 1e3,
+                          "frac_of_hbm_bound": (step_bytes / (hbm * 1e9) * 1e3) / ms_per_step},
+        "kernels_ms": {"intra": intra_avg, "scan": scan_avg},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        r, desc, thr, _ = oracle_sample_rate(x, args.ref_seconds, host_cores())
+        line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world):
+    import torch
+    names = ("q", "k", "v", "g", "beta")
+    host_in = {n: x[n].pin_memory() for n in names}
+    h0_host = x["h0"].pin_memory() if x["h0"] is not None else None
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    ht_host = torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d += 0 if h0_host is None else h0_host.numel() * 4
+    d2h = o_host.numel() * 2 + ht_host.numel() * 4
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def one():
+        for n in names:
+            d[n].copy_(host_in[n], non_blocking=True)
+        if h0_host is not None:
+            d["h0"].copy_(h0_host, non_blocking=True)
+        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+                cu_seqlens=d["cu_seqlens"], workspace=ws, out=o, final_state=ht)
+        o_host.copy_(o, non_blocking=True)
+        ht_host.copy_(ht, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return {"value": x["B"] * x["T"] * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps, "path": "pinned host -> device copies, kda_fwd, device -> pinned host"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=2.0,
+                    help="target wall seconds of one bounded oracle sample")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    return run_reference(args) if args.impl == "reference" else run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,208 @@
+"""ctypes binding of ``libkda.so`` (the C ABI in ``include/kda.h``).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  There
+is no CPU fallback: if the library cannot be loaded, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+STATUS_NAMES = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIGNMENT",
+    4: "KDA_ERR_WORKSPACE", 5: "KDA_ERR_CUDA", 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS",
+}
+
+# Every symbol the header declares (checked by the CPU test suite).
+EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
+           "kda_status_string", "kda_chunk_table", "kda_workspace_layout")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        msg = status_string(code) if _lib is not None else STATUS_NAMES.get(code, str(code))
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({msg})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("num_seqs", ctypes.c_int32)]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "seq_info", "chunk_info", "gd", "qg", "kg", "w", "u", "aqk", "total")] + [
+        ("max_chunks", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load libkda.so (building it in-tree with nvcc first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"{path} is missing; run chunked_gated_delta_gb300.build.build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        D = ctypes.POINTER(Dims)
+        sig = {
+            "kda_fwd_workspace_size": (SZ, [D]),
+            "kda_fwd": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
+            "kda_fwd_intra": (ctypes.c_int, [P, P, P, P, P, P, D, P, SZ, P]),
+            "kda_fwd_scan": (ctypes.c_int, [F32, P, P, P, D, P, SZ, P]),
+            "kda_fwd_status": (ctypes.c_int, [P, P]),
+            "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "kda_chunk_table": (I32, [P, I32, I32, P, P]),
+            "kda_workspace_layout": (ctypes.c_int, [D, ctypes.POINTER(WsLayout)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()
+
+
+def make_dims(B, T, H, K, V, num_seqs=0) -> Dims:
+    return Dims(int(B), int(T), int(H), int(K), int(V), int(num_seqs))
+
+
+def workspace_size(dims: Dims) -> int:
+    return int(load_library().kda_fwd_workspace_size(ctypes.byref(dims)))
+
+
+def workspace_layout(dims: Dims) -> WsLayout:
+    out = WsLayout()
+    rc = load_library().kda_workspace_layout(ctypes.byref(dims), ctypes.byref(out))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_workspace_layout")
+    return out
+
+
+def chunk_table(cu_seqlens, chunk: int = 64):
+    """Host chunk table: (tile_base list, t_tiles list, total) or raises ValueError."""
+    lib = load_library()
+    cu = [int(x) for x in cu_seqlens]
+    n = len(cu) - 1
+    if n < 0:
+        raise ValueError("cu_seqlens must have at least one entry")
+    cu_a = (ctypes.c_int32 * len(cu))(*cu)
+    tb = (ctypes.c_int32 * max(n, 1))()
+    tt = (ctypes.c_int32 * max(n, 1))()
+    total = lib.kda_chunk_table(cu_a, n, int(chunk), tb, tt)
+    if total < 0:
+        raise ValueError("invalid cu_seqlens / chunk")
+    return list(tb)[:n], list(tt)[:n], int(total)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc, where):
+    if rc != KDA_OK:
+        raise KdaError(rc, where)
+
+
+def _dims_of(q, v, cu_seqlens):
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    return make_dims(B, T, H, K, V, N), (B if cu_seqlens is None else N)
+
+
+def _check_inputs(q, k, v, g, beta, h0, cu_seqlens):
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("g", g, torch.float32), ("beta", beta, torch.bfloat16)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {dt}")
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_cuda or not h0.is_contiguous()):
+        raise TypeError("h0 must be a contiguous CUDA float32 tensor")
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda):
+        raise TypeError("cu_seqlens must be a CUDA int32 tensor")
+
+
+def new_workspace(dims: Dims, device):
+    import torch
+    n = workspace_size(dims)
+    if n == 0:
+        raise KdaError(1, "kda_fwd_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_state=True,
+        workspace=None, out=None, final_state=None, stream=None):
+    """KDA chunked forward on the GPU.  Returns (o, ht) (ht None if not requested).
+
+    q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32 [B,T,H,K] (natural-log decay);
+    beta: bf16 [B,T,H]; h0: fp32 [N,H,K,V] or None; cu_seqlens: int32 [N+1] on the
+    device (B must be 1) or None.  ``workspace`` (uint8 CUDA tensor) may be passed
+    to avoid an allocation per call.
+    """
+    import torch
+    _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
+    lib = load_library()
+    dims, N = _dims_of(q, v, cu_seqlens)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = K ** -0.5
+    if workspace is None:
+        workspace = new_workspace(dims, q.device)
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=torch.bfloat16, device=q.device)
+    ht = None
+    if output_final_state:
+        ht = final_state if final_state is not None else torch.empty((N, H, K, V), dtype=torch.float32,
+                                                                      device=q.device)
+    rc = lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
+                     _ptr(cu_seqlens), _ptr(o), _ptr(ht), ctypes.byref(dims), _ptr(workspace),
+                     workspace.numel(), _stream_handle(stream))
+    _check(rc, "kda_fwd")
+    return o, ht
+
+
+def fwd_intra(q, k, v, g, beta, cu_seqlens, dims: Dims, workspace, stream=None):
+    rc = load_library().kda_fwd_intra(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                      ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                      _stream_handle(stream))
+    _check(rc, "kda_fwd_intra")
+
+
+def fwd_scan(scale, h0, o, ht, dims: Dims, workspace, stream=None):
+    rc = load_library().kda_fwd_scan(float(scale), _ptr(h0), _ptr(o), _ptr(ht), ctypes.byref(dims),
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "kda_fwd_scan")
+
+
+def status(workspace, stream=None) -> int:
+    """Synchronise the stream and return the kernels' recorded status code."""
+    return int(load_library().kda_fwd_status(_ptr(workspace), _stream_handle(stream)))

@@ -1,0 +1,298 @@
+// kda_api.cu -- the C ABI (include/kda.h): argument validation, workspace
+// layout, TMA descriptor creation, the chunk planner kernel, and the launches
+// of the intra-chunk and scan kernels on the caller's stream.
+#include <cstring>
+
+#include "../../include/kda.h"
+#include "internal.h"
+#include "tensormap.h"
+
+namespace kda {
+namespace {
+
+// ---------------------------------------------------------------- planner
+// One CTA.  Validates cu_seqlens (0 = c_0 <= ... <= c_N = T), writes the
+// per-sequence table {bos, len, tile_base, tiles} and the per-chunk table
+// {row0, valid}.  tile_base is the exclusive prefix sum of ceil(len / 64),
+// the layout of "KDA源码剖析之FlashKDA（下）" (its workspace index
+// head * total_tiles + tile_base + t is kept here as (tile_base + t) * H + head,
+// i.e. chunk-major, so that one chunk's heads are adjacent).
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads)
+    kda_plan_kernel(const int32_t* __restrict__ cu, int N, int B, int T, uint8_t* __restrict__ ws,
+                    WsLayout L) {
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    SeqInfo* seqs = reinterpret_cast<SeqInfo*>(ws + L.seq_info);
+    ChunkInfo* chunks = reinterpret_cast<ChunkInfo*>(ws + L.chunk_info);
+    __shared__ int64_t part[kPlanThreads];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    const bool varlen = cu != nullptr;
+    const int nseq = varlen ? N : B;
+    const int per = (nseq + kPlanThreads - 1) / kPlanThreads;
+    const int s0 = tid * per, s1 = min(nseq, s0 + per);
+    int64_t local = 0;
+    int my_bad = 0;
+    if (varlen && tid == 0 && (cu[0] != 0 || cu[N] != T)) my_bad = 1;
+    for (int s = s0; s < s1; ++s) {
+        const int len = varlen ? cu[s + 1] - cu[s] : T;
+        if (len < 0) my_bad = 1;
+        local += len > 0 ? tiles_of(len, kChunk) : 0;
+    }
+    part[tid] = local;
+    if (my_bad) atomicOr(&bad, 1);
+    __syncthreads();
+    // inclusive Hillis-Steele scan of the per-thread tile counts
+    for (int off = 1; off < kPlanThreads; off <<= 1) {
+        const int64_t x = tid >= off ? part[tid - off] : 0;
+        __syncthreads();
+        part[tid] += x;
+        __syncthreads();
+    }
+    const int64_t total = part[kPlanThreads - 1];
+    if (total > L.max_chunks) bad = 1;  // benign race: every writer stores 1
+    __syncthreads();
+    const bool ok = bad == 0;
+    int64_t base = part[tid] - local;
+    for (int s = s0; s < s1; ++s) {
+        const int len = varlen ? cu[s + 1] - cu[s] : T;
+        const int bos = varlen ? cu[s] : s * T;
+        const int t = (ok && len > 0) ? tiles_of(len, kChunk) : 0;
+        seqs[s] = SeqInfo{bos, ok ? len : 0, (int32_t)base, t};
+        base += t;
+    }
+    __syncthreads();
+    __threadfence_block();
+    for (int64_t c = tid; c < L.max_chunks; c += kPlanThreads) {
+        ChunkInfo ci{0, 0};
+        if (ok && c < total) {
+            int lo = 0, hi = nseq - 1;  // largest s with tile_base <= c
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (seqs[mid].tile_base <= c) lo = mid;
+                else hi = mid - 1;
+            }
+            const SeqInfo q = seqs[lo];
+            const int t = (int)(c - q.tile_base);
+            ci.row0 = q.bos + t * kChunk;
+            ci.valid = min(kChunk, q.len - t * kChunk);
+        }
+        chunks[c] = ci;
+    }
+    if (tid == 0) status[0] = ok ? 0 : kStatusBadSeqlens;
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_varlen(const kda_dims* d) { return d->num_seqs > 0; }
+
+kda_status check_dims(const kda_dims* d, bool varlen) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H < 1 || d->B < 1 || d->num_seqs < 0) return KDA_ERR_INVALID_ARG;
+    if (varlen && d->B != 1) return KDA_ERR_INVALID_ARG;
+    if (d->K != 64 && d->K != 128) return KDA_ERR_UNSUPPORTED;
+    if (d->V != 64 && d->V != 128) return KDA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)d->B * d->T;
+    if (rows > INT32_MAX / 2) return KDA_ERR_UNSUPPORTED;
+    const int64_t nc = max_chunks(*d, varlen);
+    if (nc * d->H * kChunk > INT32_MAX) return KDA_ERR_UNSUPPORTED;  // TMA coordinates are int32
+    return KDA_OK;
+}
+
+kda_status check_ws(const kda_dims* d, bool varlen, void* ws, size_t bytes, WsLayout* L) {
+    *L = ws_layout(*d, varlen);
+    if (!ws || !aligned(ws, 256)) return KDA_ERR_WORKSPACE;
+    if (bytes < L->total) return KDA_ERR_WORKSPACE;
+    return KDA_OK;
+}
+
+bool map3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int inner, int H,
+          int64_t rows, uint32_t box_inner, CUtensorMapSwizzle sw) {
+    const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)H, (uint64_t)rows};
+    const uint64_t strides[2] = {(uint64_t)inner * esize, (uint64_t)inner * esize * H};
+    const uint32_t box[3] = {box_inner, 1, (uint32_t)kChunk};
+    return make_tensormap(m, dt, 3, base, dims, strides, box, sw);
+}
+
+bool map2(CUtensorMap* m, const void* base, int inner, int64_t rows) {
+    const uint64_t dims[2] = {(uint64_t)inner, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)inner * 2};
+    const uint32_t box[2] = {64, (uint32_t)kChunk};
+    return make_tensormap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+size_t kda_fwd_workspace_size(const kda_dims* dims) {
+    if (!dims) return 0;
+    const bool varlen = is_varlen(dims);
+    if (check_dims(dims, varlen) != KDA_OK) return 0;
+    return ws_layout(*dims, varlen).total;
+}
+
+kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out) {
+    if (!dims || !out) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    const WsLayout L = ws_layout(*dims, varlen);
+    out->status = L.status;
+    out->seq_info = L.seq_info;
+    out->chunk_info = L.chunk_info;
+    out->gd = L.gd;
+    out->qg = L.qg;
+    out->kg = L.kg;
+    out->w = L.w;
+    out->u = L.u;
+    out->aqk = L.aqk;
+    out->total = L.total;
+    out->max_chunks = (int32_t)L.max_chunks;
+    out->chunk = kChunk;
+    return KDA_OK;
+}
+
+int32_t kda_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int32_t chunk,
+                        int32_t* tile_base, int32_t* t_tiles) {
+    if (!cu_seqlens || num_seqs < 0 || chunk < 1 || (num_seqs > 0 && (!tile_base || !t_tiles)))
+        return -1;
+    int64_t base = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t len = cu_seqlens[s + 1] - cu_seqlens[s];
+        if (len < 0) return -1;
+        tile_base[s] = (int32_t)base;
+        t_tiles[s] = tiles_of(len, chunk);
+        base += t_tiles[s];
+        if (base > INT32_MAX) return -1;
+    }
+    return (int32_t)base;
+}
+
+kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const float* g,
+                         const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    if (varlen != (cu_seqlens != nullptr)) return KDA_ERR_INVALID_ARG;
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    WsLayout L;
+    st = check_ws(dims, varlen, workspace, workspace_bytes, &L);
+    if (st != KDA_OK) return st;
+    const int64_t rows = (int64_t)dims->B * dims->T;
+    if (varlen && !aligned(cu_seqlens, 4)) return KDA_ERR_ALIGNMENT;
+    if (rows > 0) {
+        if (!q || !k || !v || !g || !beta) return KDA_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(beta, 2))
+            return KDA_ERR_ALIGNMENT;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int N = varlen ? dims->num_seqs : dims->B;
+    kda_plan_kernel<<<1, kPlanThreads, 0, s>>>(cu_seqlens, N, dims->B, dims->T, ws, L);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    if (rows == 0 || L.max_chunks == 0) return KDA_OK;
+    IntraArgs a{};
+    bool ok = map3(&a.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims->K, dims->H, rows, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dims->K, dims->H, rows, 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dims->V, dims->H, rows, 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a.tm_g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g, dims->K, dims->H, rows,
+                    (uint32_t)dims->K, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return KDA_ERR_CUDA;
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.ws = ws;
+    a.L = L;
+    a.H = dims->H;
+    a.K = dims->K;
+    a.V = dims->V;
+    a.max_chunks = L.max_chunks;
+    if (launch_intra(a, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const kda_dims* dims,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    WsLayout L;
+    st = check_ws(dims, varlen, workspace, workspace_bytes, &L);
+    if (st != KDA_OK) return st;
+    const int64_t rows = (int64_t)dims->B * dims->T;
+    if (rows > 0 && !o) return KDA_ERR_INVALID_ARG;
+    if ((o && !aligned(o, 16)) || (h0 && !aligned(h0, 16)) || (ht && !aligned(ht, 16)))
+        return KDA_ERR_ALIGNMENT;
+    const int N = varlen ? dims->num_seqs : dims->B;
+    ScanArgs a{};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t trows = L.max_chunks * dims->H * kChunk;
+    if (trows > 0) {
+        bool ok = map2(&a.tm_w, ws + L.w, dims->K, trows);
+        ok = ok && map2(&a.tm_qg, ws + L.qg, dims->K, trows);
+        ok = ok && map2(&a.tm_kg, ws + L.kg, dims->K, trows);
+        ok = ok && map2(&a.tm_u, ws + L.u, dims->V, trows);
+        ok = ok && map2(&a.tm_aqk, ws + L.aqk, kChunk, trows);
+        if (!ok) return KDA_ERR_CUDA;
+    }
+    a.h0 = h0;
+    a.ht = ht;
+    a.o = static_cast<uint16_t*>(o);
+    a.ws = ws;
+    a.L = L;
+    a.scale = scale;
+    a.N = N;
+    a.H = dims->H;
+    a.K = dims->K;
+    a.V = dims->V;
+    if (launch_scan(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                   float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
+                   const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+    kda_status st = kda_fwd_intra(q, k, v, g, beta, cu_seqlens, dims, workspace, workspace_bytes, stream);
+    if (st != KDA_OK) return st;
+    return kda_fwd_scan(scale, h0, o, ht, dims, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd_status(const void* workspace, void* stream) {
+    if (!workspace) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word & kStatusBadSeqlens) return KDA_ERR_BAD_SEQLENS;
+    if (word & kStatusTimeout) return KDA_ERR_TIMEOUT;
+    return KDA_OK;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape (K and V must be 64 or 128)";
+    case KDA_ERR_ALIGNMENT: return "tensor base pointer not 16-byte aligned";
+    case KDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case KDA_ERR_CUDA: return "CUDA launch or driver error";
+    case KDA_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens must satisfy 0 = c0 <= c1 <= ... <= cN = T";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked forward of Kimi Delta
+ * Attention (KDA): the gated delta rule with a decay per key dimension,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,
+ *
+ * computed in chunks of 64 tokens by two CUDA kernels: an intra-chunk kernel
+ * (in-chunk cumsum of g in log2 space, the gated Aqk, the beta-weighted
+ * lower-triangular system and its inverse, w, u, qg, kg) and a fused
+ * inter-chunk state-scan + output kernel.  The chunked form is the one stated
+ * in kernel-fun "kda/_kernels/fwd_state.py" (module docstring); its host
+ * wrapper kda_cute_fwd_call takes (qg, kg, w, u, aqk, g2, h0, scale), and this
+ * ABI starts one step earlier, from the raw (q, k, v, g, beta).  Packed
+ * variable-length batches follow "KDA源码剖析之FlashKDA（下）" (sequence
+ * boundaries bos/eos from cu_seqlens, per-sequence initial/final state).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
+ *    by the caller; the library allocates no memory and keeps no pointer
+ *    after a call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Kernel
+ *    work is enqueued asynchronously on it; the return value reports argument
+ *    validation and launch errors only.  Errors found by the kernels (bad
+ *    cu_seqlens contents, a pipeline wait that timed out) are recorded in the
+ *    workspace and returned by kda_fwd_status().
+ *  - Supported shapes: K in {64, 128}, V in {64, 128}, H >= 1, T >= 0.
+ *    Other K/V return KDA_ERR_UNSUPPORTED.
+ *  - Every tensor base pointer must be 16-byte aligned (KDA_ERR_ALIGNMENT).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, inconsistent dims        */
+    KDA_ERR_UNSUPPORTED = 2,  /* K or V outside the supported set                       */
+    KDA_ERR_ALIGNMENT = 3,    /* a tensor base pointer is not 16-byte aligned           */
+    KDA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned or smaller than required    */
+    KDA_ERR_CUDA = 5,         /* a CUDA launch / driver call failed                     */
+    KDA_ERR_TIMEOUT = 6,      /* a kernel pipeline wait ran out of time (kda_fwd_status) */
+    KDA_ERR_BAD_SEQLENS = 7   /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T          */
+} kda_status;
+
+/*
+ * Problem dimensions.
+ *   Fixed length: num_seqs = 0 and cu_seqlens == NULL; B >= 1 sequences of T
+ *   tokens each (N = B).
+ *   Packed variable length: num_seqs = N >= 1 and cu_seqlens != NULL; B must
+ *   be 1 and T is the total number of tokens.
+ *   A mismatch between num_seqs and cu_seqlens is KDA_ERR_INVALID_ARG.
+ * K = key (state row) dim, V = value dim, H = heads.
+ */
+typedef struct kda_dims {
+    int32_t B, T, H, K, V;
+    int32_t num_seqs;
+} kda_dims;
+
+/*
+ * Bytes of device workspace kda_fwd needs for these dims (an upper bound that
+ * does not depend on the cu_seqlens contents).  Returns 0 for invalid dims.
+ * The workspace holds the intra-chunk intermediates qg, kg, w (bf16,
+ * [chunks, H, 64, K]), u (bf16 [chunks, H, 64, V]), Aqk (bf16 [chunks, H, 64,
+ * 64]), the per-chunk log2 decay gd (fp32 [chunks, H, K]), the chunk and
+ * sequence tables, and a status word: about 1160 bytes per token-head at
+ * K = V = 128.
+ */
+size_t kda_fwd_workspace_size(const kda_dims* dims);
+
+/*
+ * Full forward: kda_fwd_intra followed by kda_fwd_scan on the same stream.
+ *
+ *   q, k      bf16 [B, T, H, K]   queries / keys (the kernels do not normalise)
+ *   v         bf16 [B, T, H, V]
+ *   g         fp32 [B, T, H, K]   natural-log decay per key dimension (g <= 0
+ *                                 expected; any finite value is accepted)
+ *   beta      bf16 [B, T, H]      write strength, already activated (in (0,1))
+ *   scale     multiplies o only (usually K^-0.5)
+ *   h0        fp32 [N, H, K, V]   initial state per sequence, or NULL = zeros
+ *   cu_seqlens int32 [N + 1]      device, packed sequence offsets, or NULL
+ *   o         bf16 [B, T, H, V]   output (every valid token row is written)
+ *   ht        fp32 [N, H, K, V]   final state per sequence, or NULL = not stored
+ *   workspace device, >= kda_fwd_workspace_size(dims) bytes, 256-byte aligned;
+ *             its contents on entry do not matter, and it must not be shared by
+ *             calls that may run concurrently.
+ * Returns KDA_OK once both kernels are enqueued.
+ */
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                   float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
+                   const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Intra-chunk stage alone: resets the status word, builds the chunk tables
+ * from cu_seqlens (validating them), and writes qg, kg, w, u, Aqk and gd for
+ * every (chunk, head) into the workspace.  Same argument meanings as kda_fwd.
+ */
+kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const float* g,
+                         const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Inter-chunk stage alone: the serial state scan and the output, reading the
+ * intermediates that kda_fwd_intra left in `workspace` for the same dims.
+ * One CTA per (sequence, head, 64-wide V tile).
+ */
+kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const kda_dims* dims,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and returns the error the kernels recorded in
+ * `workspace` during the last kda_fwd / kda_fwd_intra / kda_fwd_scan on it
+ * (KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
+ * stream itself reports an error.
+ */
+kda_status kda_fwd_status(const void* workspace, void* stream);
+
+/* Static description of a status code.  Never NULL. */
+const char* kda_status_string(kda_status s);
+
+/*
+ * Host helper (no GPU needed): the chunk table of a packed batch, the same
+ * routine the device planner runs.  For each sequence s, t_tiles[s] =
+ * ceil((cu[s+1] - cu[s]) / chunk) and tile_base[s] = sum of t_tiles over the
+ * earlier sequences ("KDA源码剖析之FlashKDA（下）", the tile_base / t_tiles table
+ * of its sequence-information section).  Returns the total number of tiles, or
+ * -1 if the arguments are invalid (NULL, num_seqs < 0, chunk < 1, or
+ * decreasing offsets).
+ */
+int32_t kda_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int32_t chunk,
+                        int32_t* tile_base, int32_t* t_tiles);
+
+/*
+ * Byte offsets of the regions inside the workspace, for inspection of the
+ * intra-chunk intermediates (tests).  `max_chunks` is the chunk capacity
+ * the layout was sized for.  Returns KDA_ERR_INVALID_ARG for invalid dims.
+ */
+typedef struct kda_ws_layout {
+    size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, total;
+    int32_t max_chunks;
+    int32_t chunk;
+} kda_ws_layout;
+kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,116 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the header
+declares, sizes its workspace as documented, plans chunks as the pages' worked
+examples do, and rejects bad arguments before touching a GPU."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import chunked_gated_delta_gb300 as kda
+from chunked_gated_delta_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kda.load_library()
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "kda.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_header_symbol(lib):
+    names = header_functions()
+    assert names, "no functions parsed from include/kda.h"
+    for n in names:
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = kda.status_string(code)
+        assert isinstance(s, str) and s
+    assert kda.status_string(99) == "unknown status"
+
+
+def test_chunk_table_matches_flashkda_examples():
+    with open(os.path.join(GOLDEN, "flashkda_chunk_table.json")) as f:
+        ex = json.load(f)["examples"]
+    for e in ex:
+        tb, tt, total = kda.chunk_table(e["cu_seqlens"], e["chunk"])
+        assert tb == e["tile_base"] and tt == e["t_tiles"]
+        assert total == sum(e["t_tiles"])
+        if "chunk_lengths" in e:
+            L = e["cu_seqlens"][1] - e["cu_seqlens"][0]
+            lens = [min(e["chunk"], L - t * e["chunk"]) for t in range(tt[0])]
+            assert lens == e["chunk_lengths"]
+
+
+def test_chunk_table_edge_cases():
+    assert kda.chunk_table([0]) == ([], [], 0)
+    assert kda.chunk_table([0, 0, 64, 65, 65]) == ([0, 0, 1, 2], [0, 1, 1, 0], 2)
+    with pytest.raises(ValueError):
+        kda.chunk_table([0, 5, 3])
+
+
+def test_workspace_size_headline():
+    d = kda.make_dims(4, 8192, 32, 128, 128)
+    n = kda.workspace_size(d)
+    th = 4 * 8192 * 32
+    # qg, kg, w, u (4 x 256 B) + Aqk (128 B) + gd (8 B per token-head at 64-token chunks)
+    assert 1160 * th <= n <= 1160 * th + (1 << 20)
+    L = kda.workspace_layout(d)
+    assert L.max_chunks == 4 * 128 and L.chunk == 64 and L.total == n
+    offs = [L.status, L.seq_info, L.chunk_info, L.gd, L.qg, L.kg, L.w, L.u, L.aqk, L.total]
+    assert offs == sorted(offs)
+    for o in (L.gd, L.qg, L.kg, L.w, L.u, L.aqk):
+        assert o % 1024 == 0
+
+
+def test_workspace_size_varlen_bound():
+    # sum_s ceil(L_s/64) <= floor((T + 63 N) / 64)
+    d = kda.make_dims(1, 1000, 2, 64, 64, num_seqs=7)
+    L = kda.workspace_layout(d)
+    assert L.max_chunks == (1000 + 63 * 7) // 64
+    assert kda.workspace_size(kda.make_dims(1, 10, 2, 96, 64)) == 0  # unsupported K
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced on these paths
+
+
+def call_fwd(lib, dims, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, o=FAKE, ht=None,
+             ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = 1 << 40
+    P = ctypes.c_void_p
+    return lib.kda_fwd(P(q), P(k), P(v), P(g), P(beta), 0.1, P(h0), P(cu), P(o), P(ht),
+                       ctypes.byref(dims) if dims is not None else None, P(ws), ws_bytes, None)
+
+
+def test_validation_errors_before_any_launch(lib):
+    d = kda.make_dims(1, 128, 2, 128, 128)
+    assert call_fwd(lib, None) == 1                                     # NULL dims
+    assert call_fwd(lib, kda.make_dims(1, 128, 2, 96, 128)) == 2        # K unsupported
+    assert call_fwd(lib, kda.make_dims(1, 128, 2, 128, 192)) == 2       # V unsupported
+    assert call_fwd(lib, kda.make_dims(1, -1, 2, 128, 128)) == 1        # negative T
+    assert call_fwd(lib, kda.make_dims(1, 128, 0, 128, 128)) == 1       # no heads
+    assert call_fwd(lib, d, ws=0) == 4                                  # no workspace
+    assert call_fwd(lib, d, ws=FAKE + 64) == 4                          # misaligned workspace
+    assert call_fwd(lib, d, ws_bytes=1024) == 4                         # too small
+    assert call_fwd(lib, d, q=FAKE + 8) == 3                            # misaligned q
+    assert call_fwd(lib, d, g=FAKE + 4) == 3                            # misaligned g
+    assert call_fwd(lib, d, k=0) == 1                                   # NULL k
+    assert call_fwd(lib, d, cu=FAKE) == 1                               # cu_seqlens without num_seqs
+    dv = kda.make_dims(2, 128, 2, 128, 128, num_seqs=3)
+    assert call_fwd(lib, dv, cu=FAKE) == 1                              # packed batch needs B == 1
+    dv = kda.make_dims(1, 128, 2, 128, 128, num_seqs=3)
+    assert call_fwd(lib, dv, cu=None) == 1                              # num_seqs without cu_seqlens

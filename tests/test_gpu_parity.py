@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every element; the full-size workloads compare every
+element of a seeded sample of (sequence, head) units, run in the same launch
+configuration the benchmark times.  Tolerances are those of the forward with
+bf16 I/O and fp32 accumulation (parity_util.REL_O / MAXREL_O / REL_HT).
+"""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_gb300 import synth
+from parity_util import (assert_within, compare, make, oracle_ref, run_gpu, sample_units, to_dev)
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+def full_check(x, want_ht=True, what=""):
+    o, ht = run_gpu(x, want_ht=want_ht)
+    o_ref, ht_ref = oracle_ref(x, want_ht=want_ht)
+    res = compare(x, o, ht, o_ref, ht_ref)
+    assert_within(res, what)
+    return res
+
+
+# ------------------------------------------------------------------ small, every element
+
+def test_tiny_workload():
+    x = synth.make_inputs(synth.WORKLOADS["tiny"])
+    full_check(x, what="tiny")
+
+
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_small_shapes_ragged(K, V, T):
+    x = synth.make_inputs(make(B=2, T=T, H=3, K=K, V=V, seed=T * 7 + K + V))
+    full_check(x, what=f"K={K} V={V} T={T}")
+
+
+def test_no_initial_state_and_no_final_state():
+    x = synth.make_inputs(make(B=1, T=300, H=2, h0=False, seed=5))
+    full_check(x, what="h0=None")
+    x = synth.make_inputs(make(B=1, T=300, H=2, seed=6))
+    o, ht = run_gpu(x, want_ht=False)
+    assert ht is None
+    o_ref, _ = oracle_ref(x, want_ht=False)
+    assert_within(compare(x, o, None, o_ref, None), "ht not requested")
+
+
+def test_varlen_small_with_empty_and_edge_lengths():
+    lengths = [1, 0, 63, 64, 65, 130, 0, 7]
+    x = synth.make_inputs(make(T=0, H=3, seed=11), lengths=lengths)
+    x["h0"] = 0.1 * torch.randn((len(lengths), 3, 128, 128), generator=torch.Generator().manual_seed(3))
+    res = full_check(x, what="varlen small")
+    o, ht = run_gpu(x)
+    for s, L in enumerate(lengths):
+        if L == 0:
+            torch.testing.assert_close(ht[s].cpu(), x["h0"][s], rtol=0, atol=0)
+    assert res
+
+
+def test_strong_decay_takes_exact_path():
+    """Decay so strong that gate factors would overflow: the exact per-element path."""
+    x = synth.make_inputs(make(B=1, T=200, H=2, mu=-6.0, seed=21))
+    full_check(x, what="strong decay")
+
+
+def test_near_full_forget_invariant():
+    """g = -80 (a finite stand-in for -inf) and beta = 1: o_t = scale (q_t . k_t) v_t."""
+    x = synth.make_inputs(make(B=1, T=150, H=2, seed=31))
+    x["g"] = torch.full_like(x["g"], -80.0)
+    x["beta"] = torch.ones_like(x["beta"])
+    o, ht = run_gpu(x)
+    q, k, v = (x[n].double() for n in ("q", "k", "v"))
+    want = x["scale"] * (q * k).sum(-1, keepdim=True) * v
+    got = o.double().cpu()
+    err = (got - want).norm() / want.norm()
+    assert err < 5e-3, float(err)
+    o_ref, ht_ref = oracle_ref(x)
+    assert_within(compare(x, o, ht, o_ref, ht_ref), "g=-80")
+
+
+# ------------------------------------------------------------------ named workloads
+
+def test_mid_workload_full():
+    x = synth.make_inputs(synth.WORKLOADS["mid"])
+    full_check(x, what="mid")
+
+
+def test_varlen_workload_sampled():
+    x = synth.make_inputs(synth.WORKLOADS["varlen"])
+    lens = np.diff(x["cu_seqlens"].numpy())
+    units = sample_units(x, 24, seed=1,
+                         include=[(int(np.argmin(lens)), 0), (int(np.argmax(lens)), 31)])
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = oracle_ref(x, units=units)
+    assert_within(compare(x, o, ht, o_ref, ht_ref, units), "varlen")
+
+
+def test_headline_workload_sampled():
+    x = synth.make_inputs(synth.WORKLOADS["headline"])
+    units = sample_units(x, 16, seed=2, include=[(0, 0), (3, 31)])
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = oracle_ref(x, units=units)
+    assert_within(compare(x, o, ht, o_ref, ht_ref, units), "headline")
+
+
+def test_long_workload_sampled():
+    x = synth.make_inputs(synth.WORKLOADS["long"])
+    units = sample_units(x, 6, seed=3, include=[(0, 0)])
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = oracle_ref(x, units=units)
+    assert_within(compare(x, o, ht, o_ref, ht_ref, units), "long")
+
+
+# ------------------------------------------------------------------ metamorphic (bitwise)
+
+def _small():
+    return synth.make_inputs(make(B=2, T=190, H=3, seed=41))
+
+
+def test_power_of_two_scaling_is_exact():
+    x = _small()
+    o1, h1 = run_gpu(x)
+    y = dict(x, v=(x["v"].float() * 2).to(torch.bfloat16), h0=x["h0"] * 2)
+    o2, h2 = run_gpu(y)
+    assert torch.equal(o2.float(), 2 * o1.float())
+    assert torch.equal(h2, 2 * h1)
+    z = dict(x, scale=2 * x["scale"])
+    o3, h3 = run_gpu(z)
+    assert torch.equal(o3.float(), 2 * o1.float())
+    assert torch.equal(h3, h1)
+
+
+def test_head_and_batch_permutation_equivariance():
+    x = _small()
+    o1, h1 = run_gpu(x)
+    perm = torch.tensor([2, 0, 1])
+    y = dict(x)
+    for n in ("q", "k", "v", "g"):
+        y[n] = x[n][:, :, perm].contiguous()
+    y["beta"] = x["beta"][:, :, perm].contiguous()
+    y["h0"] = x["h0"][:, perm].contiguous()
+    o2, h2 = run_gpu(y)
+    assert torch.equal(o2, o1[:, :, perm])
+    assert torch.equal(h2, h1[:, perm])
+    bperm = torch.tensor([1, 0])
+    z = dict(x)
+    for n in ("q", "k", "v", "g", "beta"):
+        z[n] = x[n][bperm].contiguous()
+    z["h0"] = x["h0"][bperm].contiguous()
+    o3, h3 = run_gpu(z)
+    assert torch.equal(o3, o1[bperm])
+    assert torch.equal(h3, h1[bperm])
+
+
+def test_deterministic_and_workspace_contents_do_not_matter():
+    import chunked_gated_delta_gb300 as kda
+    x = _small()
+    d = to_dev(x)
+    dims = kda.make_dims(x["B"], x["T"], x["H"], x["K"], x["V"])
+    ws = kda.new_workspace(dims, "cuda")
+    ws.fill_(0xFF)  # NaN bit patterns everywhere
+    o1, h1 = run_gpu(x, workspace=ws)
+    ws.fill_(0x00)
+    o2, h2 = run_gpu(x, workspace=ws)
+    o3, h3 = run_gpu(x)
+    assert torch.equal(o1, o2) and torch.equal(o1, o3)
+    assert torch.equal(h1, h2) and torch.equal(h1, h3)
+    assert kda.status(ws) == 0
+    del d
+
+
+def test_causal_bitwise():
+    x = _small()
+    o1, _ = run_gpu(x)
+    t0 = 100  # inside the second chunk
+    y = dict(x)
+    gen = torch.Generator().manual_seed(9)
+    for n in ("q", "k", "v"):
+        t = x[n].clone()
+        t[:, t0 + 1:] = torch.randn(t[:, t0 + 1:].shape, generator=gen).to(t.dtype)
+        y[n] = t
+    b = x["beta"].clone()
+    b[:, t0 + 1:] = 0.5
+    y["beta"] = b
+    o2, _ = run_gpu(y)
+    assert torch.equal(o1[:, :t0 + 1], o2[:, :t0 + 1])
+    assert not torch.equal(o1[:, t0 + 1:], o2[:, t0 + 1:])
+
+
+def test_varlen_writes_only_its_rows():
+    import chunked_gated_delta_gb300 as kda
+    lengths = [70, 1, 129]
+    x = synth.make_inputs(make(T=0, H=2, seed=51), lengths=lengths)
+    d = to_dev(x)
+    T = sum(lengths)
+    big = torch.full((1, T + 64, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = big[:, :T]
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+            cu_seqlens=d["cu_seqlens"], out=o)
+    torch.cuda.synchronize()
+    assert torch.all(big[:, T:] == 7.0)
+    o_ref, _ = oracle_ref(x, want_ht=False)
+    assert_within(compare(x, o, None, o_ref, None), "varlen canary")
+
+
+def test_bad_seqlens_reported():
+    import chunked_gated_delta_gb300 as kda
+    x = synth.make_inputs(make(T=0, H=2, seed=61), lengths=[10, 20])
+    d = to_dev(x)
+    d["cu_seqlens"] = torch.tensor([0, 25, 20], dtype=torch.int32, device="cuda")  # decreasing
+    dims = kda.make_dims(1, 30, 2, 128, 128, num_seqs=2)
+    ws = kda.new_workspace(dims, "cuda")
+    o = torch.zeros((1, 30, 2, 128), dtype=torch.bfloat16, device="cuda")
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], cu_seqlens=d["cu_seqlens"],
+            workspace=ws, out=o)
+    assert kda.status(ws) == 7
+    assert torch.all(o == 0)
+
+
+def test_empty_batch_copies_h0():
+    import chunked_gated_delta_gb300 as kda
+    h0 = torch.randn((2, 3, 128, 128), device="cuda")
+    z = torch.zeros((2, 0, 3, 128), dtype=torch.bfloat16, device="cuda")
+    o, ht = kda.fwd(z, z, z, torch.zeros((2, 0, 3, 128), device="cuda"),
+                    torch.zeros((2, 0, 3), dtype=torch.bfloat16, device="cuda"), 0.1, h0=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(ht, h0)
