@@ -11,7 +11,9 @@ from .binding import (  # noqa: F401
     KdaError,
     chunk_table,
     fwd,
+    fwd_host,
     fwd_intra,
+    host_arena_size,
     fwd_scan,
     library_path,
     load_library,

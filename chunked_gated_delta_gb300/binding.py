@@ -23,7 +23,8 @@ STATUS_NAMES = {
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
-           "kda_status_string", "kda_chunk_table", "kda_workspace_layout")
+           "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
+           "kda_fwd_host")
 
 
 class KdaError(RuntimeError):
@@ -71,6 +72,8 @@ def load_library(build_if_missing: bool = True):
             "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "kda_chunk_table": (I32, [P, I32, I32, P, P]),
             "kda_workspace_layout": (ctypes.c_int, [D, ctypes.POINTER(WsLayout)]),
+            "kda_fwd_host_arena_size": (SZ, [D]),
+            "kda_fwd_host": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -206,3 +209,17 @@ def fwd_scan(scale, h0, o, ht, dims: Dims, workspace, stream=None):
 def status(workspace, stream=None) -> int:
     """Synchronise the stream and return the kernels' recorded status code."""
     return int(load_library().kda_fwd_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def host_arena_size(dims: Dims) -> int:
+    return int(load_library().kda_fwd_host_arena_size(ctypes.byref(dims)))
+
+
+def fwd_host(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, dims: Dims, arena, stream=None):
+    """kda_fwd_host: all tensors are (preferably pinned) CPU tensors; ``arena`` is a
+    uint8 CUDA tensor of at least host_arena_size(dims) bytes.  Asynchronous on
+    ``stream``; synchronise before reading o / ht."""
+    rc = load_library().kda_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                     _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(ht), ctypes.byref(dims),
+                                     _ptr(arena), arena.numel(), _stream_handle(stream))
+    _check(rc, "kda_fwd_host")

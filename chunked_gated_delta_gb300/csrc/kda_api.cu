@@ -269,6 +269,81 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, 
     return kda_fwd_scan(scale, h0, o, ht, dims, workspace, workspace_bytes, stream);
 }
 
+namespace {
+struct HostArena {
+    size_t q, k, v, g, beta, h0, cu, o, ht, ws, total;
+};
+HostArena host_arena(const kda_dims* d) {
+    const bool varlen = is_varlen(d);
+    const size_t rows = (size_t)d->B * d->T;
+    const size_t N = varlen ? (size_t)d->num_seqs : (size_t)d->B;
+    HostArena A{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 1024);
+        return at;
+    };
+    A.q = take(rows * d->H * d->K * 2);
+    A.k = take(rows * d->H * d->K * 2);
+    A.v = take(rows * d->H * d->V * 2);
+    A.g = take(rows * d->H * d->K * 4);
+    A.beta = take(rows * d->H * 2);
+    A.h0 = take(N * d->H * d->K * d->V * 4);
+    A.cu = take((N + 1) * 4);
+    A.o = take(rows * d->H * d->V * 2);
+    A.ht = take(N * d->H * d->K * d->V * 4);
+    A.ws = take(ws_layout(*d, varlen).total);
+    A.total = off;
+    return A;
+}
+}  // namespace
+
+size_t kda_fwd_host_arena_size(const kda_dims* dims) {
+    if (!dims || check_dims(dims, is_varlen(dims)) != KDA_OK) return 0;
+    return host_arena(dims).total;
+}
+
+kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, float scale, const float* h0, const int32_t* cu_seqlens,
+                        void* o, float* ht, const kda_dims* dims, void* arena, size_t arena_bytes,
+                        void* stream) {
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    if (varlen != (cu_seqlens != nullptr)) return KDA_ERR_INVALID_ARG;
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    const HostArena A = host_arena(dims);
+    if (!arena || !aligned(arena, 256) || arena_bytes < A.total) return KDA_ERR_WORKSPACE;
+    const size_t rows = (size_t)dims->B * dims->T;
+    const size_t N = varlen ? (size_t)dims->num_seqs : (size_t)dims->B;
+    if (rows > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(arena);
+    const size_t HK = (size_t)dims->H * dims->K, HV = (size_t)dims->H * dims->V;
+    const size_t state = N * dims->H * dims->K * dims->V * 4;
+    struct Cp { void* dst; const void* src; size_t bytes; };
+    const Cp in[] = {{base + A.q, q, rows * HK * 2},   {base + A.k, k, rows * HK * 2},
+                     {base + A.v, v, rows * HV * 2},   {base + A.g, g, rows * HK * 4},
+                     {base + A.beta, beta, rows * dims->H * 2},
+                     {base + A.h0, h0, h0 ? state : 0},
+                     {base + A.cu, cu_seqlens, cu_seqlens ? (N + 1) * 4 : 0}};
+    for (const Cp& c : in)
+        if (c.bytes > 0 && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    st = kda_fwd(base + A.q, base + A.k, base + A.v, reinterpret_cast<const float*>(base + A.g),
+                 base + A.beta, scale, h0 ? reinterpret_cast<const float*>(base + A.h0) : nullptr,
+                 cu_seqlens ? reinterpret_cast<const int32_t*>(base + A.cu) : nullptr, base + A.o,
+                 ht ? reinterpret_cast<float*>(base + A.ht) : nullptr, dims, base + A.ws,
+                 A.total - A.ws, stream);
+    if (st != KDA_OK) return st;
+    if (rows > 0 && cudaMemcpyAsync(o, base + A.o, rows * HV * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (ht && state > 0 && cudaMemcpyAsync(ht, base + A.ht, state, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status kda_fwd_status(const void* workspace, void* stream) {
     if (!workspace) return KDA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

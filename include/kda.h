@@ -114,6 +114,26 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * End-to-end forward from HOST buffers.  Copies q, k, v, g, beta (and h0,
+ * cu_seqlens when given) from host memory into `arena`, runs kda_fwd there,
+ * and copies o (and ht) back to host memory -- one cudaMemcpyAsync per tensor,
+ * everything enqueued on `stream`.  The caller synchronises `stream` before
+ * reading o / ht.  Host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister) for the copies to overlap; pageable memory works but the
+ * copies then block the calling thread.
+ *   All tensor pointers here are HOST pointers with the shapes and dtypes of
+ *   kda_fwd; cu_seqlens (host int32 [N+1]) may be NULL for fixed length.
+ *   arena: device memory of at least kda_fwd_host_arena_size(dims) bytes,
+ *   256-byte aligned, owned by the caller; it holds the device copies of the
+ *   inputs and outputs and the workspace.
+ */
+size_t kda_fwd_host_arena_size(const kda_dims* dims);
+kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, float scale, const float* h0, const int32_t* cu_seqlens,
+                        void* o, float* ht, const kda_dims* dims, void* arena, size_t arena_bytes,
+                        void* stream);
+
+/*
  * Synchronises `stream` and returns the error the kernels recorded in
  * `workspace` during the last kda_fwd / kda_fwd_intra / kda_fwd_scan on it
  * (KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
