@@ -228,3 +228,25 @@ def test_empty_batch_copies_h0():
                     torch.zeros((2, 0, 3), dtype=torch.bfloat16, device="cuda"), 0.1, h0=h0)
     torch.cuda.synchronize()
     assert torch.equal(ht, h0)
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    """kda_fwd_host (host buffers, copies inside) gives the same bits as kda_fwd."""
+    import chunked_gated_delta_gb300 as kda
+    for x in (synth.make_inputs(make(B=2, T=130, H=2, seed=81)),
+              synth.make_inputs(make(T=0, H=2, seed=82), lengths=[5, 70, 64])):
+        o_dev, ht_dev = run_gpu(x)
+        N = x["N"]
+        dims = kda.make_dims(x["B"], x["T"], x["H"], x["K"], x["V"],
+                             0 if x["cu_seqlens"] is None else N)
+        arena = torch.empty(kda.host_arena_size(dims), dtype=torch.uint8, device="cuda")
+        pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        h0 = x["h0"].pin_memory() if x["h0"] is not None else None
+        cu = x["cu_seqlens"].pin_memory() if x["cu_seqlens"] is not None else None
+        o = torch.empty((x["B"], x["T"], x["H"], x["V"]), dtype=torch.bfloat16, pin_memory=True)
+        ht = torch.empty((N, x["H"], x["K"], x["V"]), dtype=torch.float32, pin_memory=True)
+        kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], x["scale"], h0, cu, o, ht,
+                     dims, arena)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_dev.cpu())
+        assert torch.equal(ht, ht_dev.cpu())
