@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     fwd,
     fwd_host,
     fwd_intra,
+    fwd_noalloc,
     host_arena_size,
     fwd_scan,
     library_path,

@@ -24,7 +24,7 @@ STATUS_NAMES = {
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
-           "kda_fwd_host")
+           "kda_fwd_host", "kda_fwd_noalloc")
 
 
 class KdaError(RuntimeError):
@@ -74,6 +74,7 @@ def load_library(build_if_missing: bool = True):
             "kda_workspace_layout": (ctypes.c_int, [D, ctypes.POINTER(WsLayout)]),
             "kda_fwd_host_arena_size": (SZ, [D]),
             "kda_fwd_host": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
+            "kda_fwd_noalloc": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -223,3 +224,19 @@ def fwd_host(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, dims: Dims, arena, 
                                      _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(ht), ctypes.byref(dims),
                                      _ptr(arena), arena.numel(), _stream_handle(stream))
     _check(rc, "kda_fwd_host")
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
+
+
+def fwd_noalloc(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, stream=None):
+    """kda_fwd_noalloc: the forward with the library's built-in scratch array as
+    workspace (no device allocation by the library).  All tensors are CUDA
+    tensors allocated by the caller; o and ht are written in place."""
+    _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
+    dims, _ = _dims_of(q, v, cu_seqlens)
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    rc = load_library().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                        _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(ht),
+                                        ctypes.byref(dims), _stream_handle(stream))
+    _check(rc, "kda_fwd_noalloc")

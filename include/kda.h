@@ -134,6 +134,45 @@ kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float
                         void* stream);
 
 /*
+ * Scratch capacity of kda_fwd_noalloc: 64 MiB, enough for the workspace of
+ * about 56 thousand token-heads at K = V = 128 (e.g. T = 1792 tokens with
+ * H = 32, or T = 57344 with H = 1).
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * kda_fwd without a caller workspace (the method's pages have no counterpart:
+ * this is an interface convenience of this library).  Meant for callers that
+ * cannot call cudaMalloc: a plugin running inside a host framework whose
+ * caching allocator owns all of the GPU's memory and must not be bypassed,
+ * and latency-critical paths where cudaMalloc / cudaFree would implicitly
+ * synchronise the device.  The workspace lives instead in a file-scope
+ * device array of KDA_NOALLOC_SCRATCH_BYTES that every GPU which loads the
+ * library holds until the process exits.  This call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *   Arguments are those of kda_fwd minus the workspace; the caller still
+ *   passes every input and output buffer.
+ *   Problems whose workspace (kda_fwd_workspace_size) exceeds the scratch
+ *   capacity return KDA_ERR_WORKSPACE before anything is enqueued.
+ *   The first call on each device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress) and caches it; make that first
+ *   call before any stream capture begins.
+ *   All calls share the one array, which keeps the previous call's contents.
+ *   The forward needs nothing in it to start at zero (the planner rewrites
+ *   the status word and tables on every call).  Calls that may overlap on the
+ *   GPU (different streams, or different host threads) race on the array and
+ *   must be serialised by the caller.
+ *   Errors that only the kernels can detect (bad cu_seqlens contents, a
+ *   timed-out pipeline wait) are recorded in the array's status word, which
+ *   this call does not expose: a caller that needs them uses kda_fwd with a
+ *   workspace and kda_fwd_status.
+ */
+kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, float scale, const float* h0,
+                           const int32_t* cu_seqlens, void* o, float* ht, const kda_dims* dims,
+                           void* stream);
+
+/*
  * Synchronises `stream` and returns the error the kernels recorded in
  * `workspace` during the last kda_fwd / kda_fwd_intra / kda_fwd_scan on it
  * (KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
