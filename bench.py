@@ -58,7 +58,6 @@ def bytes_per_token_head(K, V, C=64):
 
 def flops_per_token_head(K, V, C=64):
     """Chunked-form flops per token-head (Aqk, A, w, u; WH, qg@h, kg^T v'; Aqk@v')."""
-    per_chunk = 4 * 2 * C * C * K / 2 + 0 * 0  # Aqk/A (2 C^2 K each) + w (2 C^2 K) + u (2 C^2 V)
     per_chunk = 2 * C * C * K * 3 + 2 * C * C * V + 3 * 2 * C * K * V + 2 * C * C * V
     return per_chunk / C
 
@@ -305,7 +304,7 @@ def run_gb300(args):
     step_flops = flops_per_token_head(K, V) * th
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world)
+    e2e = run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world) if args.e2e_steps > 0 else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

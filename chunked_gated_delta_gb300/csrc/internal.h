@@ -10,7 +10,8 @@
 namespace kda {
 
 struct IntraArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;  // user inputs, 3-D {dim, H, rows}
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;      // user inputs, 3-D {dim, H, rows}
+    CUtensorMap st_qg, st_w, st_u, st_aqk;   // workspace tiles (stores), 2-D {dim, tiles*64}
     const uint16_t* beta;                // bf16 bits [rows, H]
     uint8_t* ws;
     WsLayout L;

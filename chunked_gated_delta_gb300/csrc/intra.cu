@@ -16,19 +16,24 @@
 //   T        = (I + A)^-1,   T' = T diag(beta)
 //   w        = T' (k * exp2(g2)),   u = T' v         -> workspace
 //
-// GB300 mapping:
+// GB300 mapping (256 threads; every phase uses all eight warps):
 //  * q, k, v arrive by TMA (3-D maps over [rows, H, dim], 128-byte swizzle)
 //    straight into the layouts the tensor core reads; g (fp32) by an
-//    unswizzled TMA tile.  Rows past the end of the sequence are zeroed
-//    on chip, so padding rows are inert (g = 0, beta = 0, q = k = v = 0).
+//    unswizzled TMA tile.  Rows past the end of the sequence are zeroed on
+//    chip, so padding rows are inert (g = 0, beta = 0, q = k = v = 0).
+//  * The cumsum runs as two passes of segment sums (P threads per key dim).
 //  * Gated products use one gate factorisation, (q exp2(g2)) . (k exp2(-g2)),
 //    so Aqk and the k.k^T Gram matrix come out of ONE tcgen05 MMA with M = 128
 //    (A operand = [qg ; k exp2(g2)] stacked, B = k exp2(-g2)), accumulated in
-//    TMEM.  If a chunk's log2 decay span exceeds kSafeSpanLog2 (factors would
+//    TMEM.  If a chunk's |g2| exceeds kSafeSpanLog2 anywhere (factors would
 //    overflow), that chunk computes the gated sums exactly per element instead.
-//  * T is found by a right-looking forward substitution in fp32, one column
-//    per thread.  w and u are two more M = 128 MMAs with A = [T' ; unused
-//    rows], reading k exp2(g2) and v as MN-major B operands in place.
+//  * T is found block-wise in fp32: the four 16x16 diagonal blocks by
+//    forward substitution, then the off-diagonal blocks level by level,
+//    T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ, spread over all threads.
+//  * w and u are two more M = 128 MMAs with A = [T' ; unused rows], reading
+//    k exp2(g2) and v as MN-major B operands in place.
+//  * qg, Aqk, w and u leave through TMA stores from swizzled shared memory;
+//    kg and gd through coalesced 16-byte stores.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -40,7 +45,7 @@ namespace {
 using namespace ptx;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kAmStride = 68;  // fp32 row stride of the A^T matrix in smem (bank spread)
+constexpr int kS = 68;  // fp32 row stride of the 64x64 matrices in smem (bank spread)
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -56,26 +61,35 @@ __device__ __forceinline__ float bf16_at(const uint8_t* p) {
 template <int KB, int VB>
 struct IntraSmem {
     static constexpr int K = 64 * KB, V = 64 * VB;
-    static constexpr uint32_t QK = 0;                   // per kb: [q / qg 8K | k / k*exp2(g2) 8K]
-    static constexpr uint32_t TP = QK + 2 * KB * 8192;  // T' bf16 [64 i][64 j], SW128 K-major
-    static constexpr uint32_t KINV = TP + 8192;         // k*exp2(-g2) per kb [64][64]; then A^T fp32
-    static constexpr uint32_t KINV_BYTES = 18432;       // >= max(KB*8192, 64*68*4)
-    static constexpr uint32_t VS = KINV + KINV_BYTES;   // v per vb [64][64], SW128
-    static constexpr uint32_t G = VS + VB * 8192;       // g then g2, fp32 [64][K]
-    static constexpr uint32_t GD = G + 64 * K * 4;      // G, fp32 [K]
-    static constexpr uint32_t BETA = GD + K * 4;        // beta, fp32 [64]
+    static constexpr uint32_t QK = 0;                   // per kb: [q / qg 8K | k / k*exp2(g2) 8K]; later w staging
+    static constexpr uint32_t TP = QK + 2 * KB * 8192;  // Aqk staging, then T' bf16 [64 i][64 j] SW128
+    static constexpr uint32_t KINV = TP + 8192;         // k*exp2(-g2) per kb [64][64]; then A^T fp32 [64][kS]
+    static constexpr uint32_t KINV_BYTES = 18432;       // >= max(KB*8192, 64*kS*4)
+    static constexpr uint32_t VS = KINV + KINV_BYTES;   // v per vb [64][64] SW128; later u staging
+    static constexpr uint32_t G = VS + VB * 8192;       // g then g2, fp32 [64][K]; later T fp32 [64][kS] + X
+    static constexpr uint32_t XS = G + 64 * kS * 4;     // X blocks fp32 [3][16][16]
+    static constexpr uint32_t G_BYTES = (64 * K * 4 > 64 * kS * 4 + 3 * 1024) ? 64 * K * 4 : 64 * kS * 4 + 3 * 1024;
+    static constexpr uint32_t GD = G + G_BYTES;         // G, fp32 [K]
+    static constexpr uint32_t EG = GD + K * 4;          // exp2(G), fp32 [K]
+    static constexpr uint32_t PART = EG + K * 4;        // cumsum segment sums, fp32 [4][K]
+    static constexpr uint32_t BETA = PART + 4 * K * 4;  // beta, fp32 [64]
     static constexpr uint32_t BYTES = BETA + 256;
     static constexpr uint32_t TX_BYTES = (2 * KB + VB) * 8192 + 64 * K * 4;
+    static_assert(XS + 3 * 256 * 4 <= GD, "T and X must fit in the g2 region");
 };
 
 template <int KB, int VB>
 __global__ void __launch_bounds__(256, 2)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                     const __grid_constant__ CUtensorMap st_qg, const __grid_constant__ CUtensorMap st_w,
+                     const __grid_constant__ CUtensorMap st_u, const __grid_constant__ CUtensorMap st_aqk,
                      const uint16_t* __restrict__ beta, uint8_t* __restrict__ ws, const WsLayout L,
                      const int H) {
     using S = IntraSmem<KB, VB>;
     constexpr int K = S::K, V = S::V;
+    constexpr int P = 256 / K;   // threads per key dim in the cumsum
+    constexpr int R = 64 / P;    // rows per cumsum segment
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -90,9 +104,14 @@ __global__ void __launch_bounds__(256, 2)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int valid = ci.valid, row0 = ci.row0;
+    const int trow = static_cast<int>(tile * 64);  // first row of this tile in the workspace maps
     const uint32_t sbase = smem_u32(sm);
     float* G = reinterpret_cast<float*>(sm + S::G);
+    float* Tsm = reinterpret_cast<float*>(sm + S::G);  // reuses the g2 region after the gating
+    float* Xsm = reinterpret_cast<float*>(sm + S::XS);
     float* GDs = reinterpret_cast<float*>(sm + S::GD);
+    float* EGs = reinterpret_cast<float*>(sm + S::EG);
+    float* PARTs = reinterpret_cast<float*>(sm + S::PART);
     float* beta_s = reinterpret_cast<float*>(sm + S::BETA);
     float* AMT = reinterpret_cast<float*>(sm + S::KINV);  // A^T [m][i], valid after the Gram step
 
@@ -125,31 +144,47 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     bool timed_out = false;
-    if (!mbar_wait(&bar_load, 0, kWaitLimitNs)) timed_out = true;
+    if (warp == 0 && !mbar_wait(&bar_load, 0, kWaitLimitNs)) timed_out = true;
+    __syncthreads();
 
-    // ---- 1. in-chunk cumsum of g, log2 space; G; overflow guard --------------
+    // ---- 1. in-chunk cumsum of g (log2 space), two passes of segment sums ---
+    const int cd = tid % K, cp = tid / K;  // key dim, segment
+    {
+        float s = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = cp * R + r;
+            s += (i < valid) ? G[i * K + cd] : 0.f;
+        }
+        PARTs[cp * K + cd] = s;
+    }
+    __syncthreads();
     bool unsafe = false;
-    if (tid < K) {
-        float acc = 0.f, mx = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 64; ++i) {
-            const float gi = (i < valid) ? G[i * K + tid] : 0.f;
-            acc += gi;
+    {
+        float acc = 0.f;
+        for (int p = 0; p < cp; ++p) acc += PARTs[p * K + cd];
+        float mx = fabsf(acc * kLog2e);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = cp * R + r;
+            acc += (i < valid) ? G[i * K + cd] : 0.f;
             const float g2 = acc * kLog2e;
-            G[i * K + tid] = g2;
+            G[i * K + cd] = g2;
             mx = fmaxf(mx, fabsf(g2));
         }
-        const float Gd = acc * kLog2e;
-        GDs[tid] = Gd;
-        reinterpret_cast<float*>(ws + L.gd)[tile * K + tid] = Gd;
+        if (cp == P - 1) {
+            const float Gd = acc * kLog2e;
+            GDs[cd] = Gd;
+            EGs[cd] = ex2(Gd);
+            reinterpret_cast<float*>(ws + L.gd)[tile * K + cd] = Gd;
+        }
         unsafe = !(mx <= kSafeSpanLog2);
     }
     const bool exact_path = __syncthreads_or(unsafe) != 0;
 
-    uint16_t* aqk_g = reinterpret_cast<uint16_t*>(ws + L.aqk) + tile * 64 * 64;
-
     // ---- 1b. (rare) exact gated sums for chunks with extreme decay -----------
     if (exact_path) {
+        uint16_t* aqk_st = reinterpret_cast<uint16_t*>(sm + S::TP);
         for (int e = tid; e < 64 * 64; e += 256) {
             const int i = e >> 6, j = e & 63;
             float sq = 0.f, sk = 0.f;
@@ -164,15 +199,14 @@ __global__ void __launch_bounds__(256, 2)
                     sk = fmaf(ki * kj, gate, sk);
                 }
             }
-            aqk_g[i * 64 + j] = __bfloat16_as_ushort(__float2bfloat16_rn(sq));
-            AMT[j * kAmStride + i] = (j < i) ? beta_s[i] * sk : 0.f;
+            aqk_st[sw128_offset(i, j) >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(sq));
+            AMT[j * kS + i] = (j < i) ? beta_s[i] * sk : 0.f;
         }
         __syncthreads();
     }
 
-    // ---- 2. gate the operands in place; qg and kg to the workspace -----------
+    // ---- 2. gate the operands in place; kg to the workspace ------------------
     {
-        uint16_t* qg_g = reinterpret_cast<uint16_t*>(ws + L.qg) + tile * 64 * K;
         uint16_t* kg_g = reinterpret_cast<uint16_t*>(ws + L.kg) + tile * 64 * K;
         constexpr int CPR = 8 * KB;  // 16-byte chunks per row
         for (int e = tid; e < 64 * CPR; e += 256) {
@@ -183,32 +217,45 @@ __global__ void __launch_bounds__(256, 2)
             const int d0 = kb * 64 + cc * 8;
             const float4 ga = *reinterpret_cast<const float4*>(G + i * K + d0);
             const float4 gb = *reinterpret_cast<const float4*>(G + i * K + d0 + 4);
-            const float4 Ga = *reinterpret_cast<const float4*>(GDs + d0);
-            const float4 Gb = *reinterpret_cast<const float4*>(GDs + d0 + 4);
             const float g2[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-            const float Gv[8] = {Ga.x, Ga.y, Ga.z, Ga.w, Gb.x, Gb.y, Gb.z, Gb.w};
             uint4 qv = *qp, kv = *kp;
             if (i >= valid) qv = kv = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
             uint32_t o_qg[4], o_kga[4], o_kin[4], o_kg[4];
+            if (!exact_path) {
+                const float4 ea = *reinterpret_cast<const float4*>(EGs + d0);
+                const float4 eb = *reinterpret_cast<const float4*>(EGs + d0 + 4);
+                const float eG[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float q0 = bf_lo(qw[t]), q1 = bf_hi(qw[t]);
-                const float k0 = bf_lo(kw[t]), k1 = bf_hi(kw[t]);
-                const float a0 = g2[2 * t], a1 = g2[2 * t + 1];
-                const float e0 = ex2(a0), e1 = ex2(a1);
-                o_qg[t] = pack_bf16x2(q0 * e0, q1 * e1);
-                o_kga[t] = pack_bf16x2(k0 * e0, k1 * e1);
-                o_kin[t] = pack_bf16x2(k0 * ex2(-a0), k1 * ex2(-a1));
-                o_kg[t] = pack_bf16x2(k0 * ex2(Gv[2 * t] - a0), k1 * ex2(Gv[2 * t + 1] - a1));
-            }
-            const uint4 vqg = make_uint4(o_qg[0], o_qg[1], o_qg[2], o_qg[3]);
-            *qp = vqg;
-            *kp = make_uint4(o_kga[0], o_kga[1], o_kga[2], o_kga[3]);
-            if (!exact_path)
+                for (int t = 0; t < 4; ++t) {
+                    const float q0 = bf_lo(qw[t]), q1 = bf_hi(qw[t]);
+                    const float k0 = bf_lo(kw[t]), k1 = bf_hi(kw[t]);
+                    const float e0 = ex2(g2[2 * t]), e1 = ex2(g2[2 * t + 1]);
+                    const float n0 = ex2(-g2[2 * t]), n1 = ex2(-g2[2 * t + 1]);
+                    o_qg[t] = pack_bf16x2(q0 * e0, q1 * e1);
+                    o_kga[t] = pack_bf16x2(k0 * e0, k1 * e1);
+                    o_kin[t] = pack_bf16x2(k0 * n0, k1 * n1);
+                    o_kg[t] = pack_bf16x2((k0 * n0) * eG[2 * t], (k1 * n1) * eG[2 * t + 1]);
+                }
                 *reinterpret_cast<uint4*>(sm + S::KINV + kb * 8192 + off) =
                     make_uint4(o_kin[0], o_kin[1], o_kin[2], o_kin[3]);
-            *reinterpret_cast<uint4*>(qg_g + i * K + d0) = vqg;
+            } else {
+                const float4 Ga = *reinterpret_cast<const float4*>(GDs + d0);
+                const float4 Gb = *reinterpret_cast<const float4*>(GDs + d0 + 4);
+                const float Gv[8] = {Ga.x, Ga.y, Ga.z, Ga.w, Gb.x, Gb.y, Gb.z, Gb.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float q0 = bf_lo(qw[t]), q1 = bf_hi(qw[t]);
+                    const float k0 = bf_lo(kw[t]), k1 = bf_hi(kw[t]);
+                    const float e0 = ex2(g2[2 * t]), e1 = ex2(g2[2 * t + 1]);
+                    o_qg[t] = pack_bf16x2(q0 * e0, q1 * e1);
+                    o_kga[t] = pack_bf16x2(k0 * e0, k1 * e1);
+                    o_kg[t] = pack_bf16x2(k0 * ex2(Gv[2 * t] - g2[2 * t]),
+                                          k1 * ex2(Gv[2 * t + 1] - g2[2 * t + 1]));
+                }
+            }
+            *qp = make_uint4(o_qg[0], o_qg[1], o_qg[2], o_qg[3]);
+            *kp = make_uint4(o_kga[0], o_kga[1], o_kga[2], o_kga[3]);
             *reinterpret_cast<uint4*>(kg_g + i * K + d0) = make_uint4(o_kg[0], o_kg[1], o_kg[2], o_kg[3]);
         }
         for (int e = tid; e < (64 - valid) * 8 * VB; e += 256) {
@@ -220,6 +267,11 @@ __global__ void __launch_bounds__(256, 2)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) tma_store_2d(&st_qg, sm + S::QK + kb * 16384, kb * 64, trow);
+        bulk_commit();
+    }
 
     uint32_t mma_phase = 0;
     // ---- 3. Gram MMA: [qg ; k exp2(g2)] @ (k exp2(-g2))^T -> TMEM ------------
@@ -238,74 +290,140 @@ __global__ void __launch_bounds__(256, 2)
                 mma_commit(&bar_mma);
             }
             __syncwarp();
+            if (!mbar_wait(&bar_mma, mma_phase, kWaitLimitNs)) timed_out = true;
         }
-        if (!mbar_wait(&bar_mma, mma_phase, kWaitLimitNs)) timed_out = true;
         mma_phase ^= 1;
+        __syncthreads();
         tc_fence_after();
-        if (warp < 2) {
-            // lanes 0..63: rows of q.k -> Aqk (lower triangle with diagonal)
-            const int i = warp * 32 + lane;
-            uint16_t* dst = aqk_g + i * 64;
+        {
+            // warp w: TMEM lane quadrant w & 3, column half w >> 2
+            const int quad = warp & 3, c0 = (warp >> 2) * 32;
+            float r[32];
+            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, r);
+            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0 + 16, r + 16);
+            tmem_ld_wait();
+            if (quad < 2) {
+                // rows of q.k -> Aqk staging (lower triangle with diagonal), SW128 [64][64] bf16
+                const int i = quad * 32 + lane;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float r[16];
-                tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, r);
-                tmem_ld_wait();
-                uint32_t wv[8];
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t wv[4];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const float lo = (c0 + 2 * t <= i) ? r[2 * t] : 0.f;
-                    const float hi = (c0 + 2 * t + 1 <= i) ? r[2 * t + 1] : 0.f;
-                    wv[t] = pack_bf16x2(lo, hi);
+                    for (int t = 0; t < 4; ++t) {
+                        const int j = c0 + cc * 8 + 2 * t;
+                        wv[t] = pack_bf16x2(j <= i ? r[cc * 8 + 2 * t] : 0.f, j + 1 <= i ? r[cc * 8 + 2 * t + 1] : 0.f);
+                    }
+                    const int chunk = (c0 >> 3) + cc;
+                    *reinterpret_cast<uint4*>(sm + S::TP + i * 128 + ((chunk ^ (i & 7)) << 4)) =
+                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
-                reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-            }
-        } else if (warp < 4) {
-            // lanes 64..127: rows of k.k -> A^T (strictly lower A, beta on the row)
-            const int i = (warp - 2) * 32 + lane;
-            const float b = beta_s[i];
+            } else {
+                // rows of k.k -> A^T (strictly lower A, beta on the row)
+                const int i = (quad - 2) * 32 + lane;
+                const float b = beta_s[i];
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float r[16];
-                tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
+                for (int t = 0; t < 32; ++t) {
                     const int j = c0 + t;
-                    AMT[j * kAmStride + i] = (j < i) ? b * r[t] : 0.f;
+                    AMT[j * kS + i] = (j < i) ? b * r[t] : 0.f;
                 }
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
     }
+    if (tid == 0) {
+        tma_store_2d(&st_aqk, sm + S::TP, 0, trow);
+        bulk_commit();
+    }
 
-    // ---- 4. T = (I + A)^-1, right-looking, one column per thread; T' = T diag(beta)
+    // ---- 4. T = (I + A)^-1 by 16x16 blocks, fp32 ------------------------------
+    // level 0: diagonal blocks by forward substitution (column per thread)
     if (tid < 64) {
-        const int j = tid;
-        float acc[64];
+        const int I = tid >> 4, cc = tid & 15, b0 = 16 * I;
+        float acc[16];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = (i == j) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 0; m < 63; ++m) {
+        for (int m = 0; m < 15; ++m) {
             const float tm = acc[m];
-            const float* arow = AMT + m * kAmStride;  // A[i][m] for all i (zero for i <= m)
+            const float* arow = AMT + (b0 + m) * kS + b0;  // A[b0 + r][b0 + m], zero for r <= m
 #pragma unroll
-            for (int i4 = ((m + 1) / 4) * 4; i4 < 64; i4 += 4) {
-                const float4 a = *reinterpret_cast<const float4*>(arow + i4);
-                acc[i4 + 0] = fmaf(-a.x, tm, acc[i4 + 0]);
-                acc[i4 + 1] = fmaf(-a.y, tm, acc[i4 + 1]);
-                acc[i4 + 2] = fmaf(-a.z, tm, acc[i4 + 2]);
-                acc[i4 + 3] = fmaf(-a.w, tm, acc[i4 + 3]);
+            for (int r4 = ((m + 1) / 4) * 4; r4 < 16; r4 += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(arow + r4);
+                acc[r4 + 0] = fmaf(-a.x, tm, acc[r4 + 0]);
+                acc[r4 + 1] = fmaf(-a.y, tm, acc[r4 + 1]);
+                acc[r4 + 2] = fmaf(-a.z, tm, acc[r4 + 2]);
+                acc[r4 + 3] = fmaf(-a.w, tm, acc[r4 + 3]);
             }
         }
-        const float bj = beta_s[j];
-        uint8_t* TP = sm + S::TP;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            *reinterpret_cast<uint16_t*>(TP + sw128_offset(i, j)) =
-                __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * bj));
+        for (int r = 0; r < 16; ++r) Tsm[(b0 + r) * kS + b0 + cc] = acc[r];
+    }
+    __syncthreads();
+    // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev
+#pragma unroll 1
+    for (int lev = 1; lev < 4; ++lev) {
+        const int nblk = 4 - lev;
+        const bool act = tid < nblk * 64;
+        const int J = tid >> 6, I = J + lev, r = (tid & 63) >> 2, c4 = (tid & 3) * 4;
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int Kb = J; Kb < I; ++Kb) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float a = AMT[(16 * Kb + m) * kS + 16 * I + r];
+                    const float4 t = *reinterpret_cast<const float4*>(Tsm + (16 * Kb + m) * kS + 16 * J + c4);
+                    acc.x = fmaf(a, t.x, acc.x);
+                    acc.y = fmaf(a, t.y, acc.y);
+                    acc.z = fmaf(a, t.z, acc.z);
+                    acc.w = fmaf(a, t.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4*>(Xsm + J * 256 + r * 16 + c4) = acc;
+        }
+        __syncthreads();
+        if (act) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* trow = Tsm + (16 * I + r) * kS + 16 * I;
+#pragma unroll
+            for (int m4 = 0; m4 < 16; m4 += 4) {
+                const float4 tv = *reinterpret_cast<const float4*>(trow + m4);
+                const float tt[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(Xsm + J * 256 + (m4 + q) * 16 + c4);
+                    acc.x = fmaf(tt[q], x.x, acc.x);
+                    acc.y = fmaf(tt[q], x.y, acc.y);
+                    acc.z = fmaf(tt[q], x.z, acc.z);
+                    acc.w = fmaf(tt[q], x.w, acc.w);
+                }
+            }
+            *reinterpret_cast<float4*>(Tsm + (16 * I + r) * kS + 16 * J + c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
+    }
+    // T' = T diag(beta) -> bf16, K-major SW128 [64 i][64 j] (the Aqk store must have read TP)
+    if (tid == 0) bulk_wait_read0();
+    __syncthreads();
+    {
+        const int i = tid >> 2, j0 = (tid & 3) * 16;
+        const float* trow = Tsm + i * kS + j0;
+        uint32_t wv[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t = *reinterpret_cast<const float4*>(trow + 4 * q);
+            const float4 b = *reinterpret_cast<const float4*>(beta_s + j0 + 4 * q);
+            const int j = j0 + 4 * q;
+            wv[2 * q] = pack_bf16x2(j <= i ? t.x * b.x : 0.f, j + 1 <= i ? t.y * b.y : 0.f);
+            wv[2 * q + 1] = pack_bf16x2(j + 2 <= i ? t.z * b.z : 0.f, j + 3 <= i ? t.w * b.w : 0.f);
+        }
+        const int ch = j0 >> 3;
+        *reinterpret_cast<uint4*>(sm + S::TP + i * 128 + ((ch ^ (i & 7)) << 4)) =
+            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        *reinterpret_cast<uint4*>(sm + S::TP + i * 128 + (((ch + 1) ^ (i & 7)) << 4)) =
+            make_uint4(wv[4], wv[5], wv[6], wv[7]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -328,31 +446,48 @@ __global__ void __launch_bounds__(256, 2)
             mma_commit(&bar_mma);
         }
         __syncwarp();
+        if (!mbar_wait(&bar_mma, mma_phase, kWaitLimitNs)) timed_out = true;
     }
-    if (!mbar_wait(&bar_mma, mma_phase, kWaitLimitNs)) timed_out = true;
+    if (tid == 0) bulk_wait_read0();  // the qg store has read QK before w is staged there
+    __syncthreads();
     tc_fence_after();
 
-    // ---- 6. w (warps 0,1) and u (warps 4,5) rows to the workspace -------------
+    // ---- 6. w (warps 0,1) and u (warps 4,5) rows -> swizzled staging -> TMA ---
     if (warp < 2 || warp == 4 || warp == 5) {
         const int quad = warp & 3, i = quad * 32 + lane;
         const bool is_w = warp < 2;
-        const int ncol = is_w ? K : V;
+        const int nblk = is_w ? KB : VB;
         const uint32_t col0 = is_w ? 0u : (uint32_t)K;
-        uint16_t* dst = is_w ? reinterpret_cast<uint16_t*>(ws + L.w) + (tile * 64 + i) * K
-                             : reinterpret_cast<uint16_t*>(ws + L.u) + (tile * 64 + i) * V;
-        for (int c0 = 0; c0 < ncol; c0 += 16) {
-            float r[16];
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + col0 + c0, r);
-            tmem_ld_wait();
-            uint32_t wv[8];
+        uint8_t* stg = sm + (is_w ? S::QK : S::VS);
+        for (int blk = 0; blk < nblk; ++blk) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) wv[t] = pack_bf16x2(r[2 * t], r[2 * t + 1]);
-            reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+            for (int half = 0; half < 2; ++half) {
+                float r[32];
+                const uint32_t col = col0 + blk * 64 + half * 32;
+                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + col, r);
+                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + col + 16, r + 16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int chunk = half * 4 + cc;
+                    *reinterpret_cast<uint4*>(stg + blk * 8192 + i * 128 + ((chunk ^ (i & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(r[cc * 8 + 0], r[cc * 8 + 1]), pack_bf16x2(r[cc * 8 + 2], r[cc * 8 + 3]),
+                                   pack_bf16x2(r[cc * 8 + 4], r[cc * 8 + 5]), pack_bf16x2(r[cc * 8 + 6], r[cc * 8 + 7]));
+                }
+            }
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) tma_store_2d(&st_w, sm + S::QK + kb * 8192, kb * 64, trow);
+#pragma unroll
+        for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::VS + vb * 8192, vb * 64, trow);
+        bulk_commit();
+        bulk_wait0();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -369,7 +504,8 @@ cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t ctas = a.max_chunks * a.H;
     if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, 256, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_g, a.beta, a.ws, a.L, a.H);
+    kern<<<(unsigned)ctas, 256, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_g, a.st_qg, a.st_w, a.st_u,
+                                                a.st_aqk, a.beta, a.ws, a.L, a.H);
     return cudaGetLastError();
 }
 

@@ -210,6 +210,11 @@ kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const floa
                     CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && map3(&a.tm_g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g, dims->K, dims->H, rows,
                     (uint32_t)dims->K, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int64_t trows = L.max_chunks * dims->H * kChunk;
+    ok = ok && map2(&a.st_qg, ws + L.qg, dims->K, trows);
+    ok = ok && map2(&a.st_w, ws + L.w, dims->K, trows);
+    ok = ok && map2(&a.st_u, ws + L.u, dims->V, trows);
+    ok = ok && map2(&a.st_aqk, ws + L.aqk, kChunk, trows);
     if (!ok) return KDA_ERR_CUDA;
     a.beta = static_cast<const uint16_t*>(beta);
     a.ws = ws;

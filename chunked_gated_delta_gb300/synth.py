@@ -52,6 +52,9 @@ WORKLOADS = {
     "varlen": Workload("varlen", B=1, T=0, H=32, K=128, V=128, varlen=16, seed=20261205),
     "long": Workload("long", B=1, T=65536, H=32, K=128, V=128, mu=5.0, h0=False,
                      seed=20261206),
+    # a quarter of the headline batch: the size profiler captures run on (its
+    # inputs, ~0.4 GB, still exceed L2)
+    "quarter": Workload("quarter", B=1, T=8192, H=32, K=128, V=128, seed=20261207),
 }
 
 
