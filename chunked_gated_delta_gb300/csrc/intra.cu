@@ -29,7 +29,8 @@
 //    overflow), that chunk computes the gated sums exactly per element instead.
 //  * T is found block-wise in fp32: the four 16x16 diagonal blocks by
 //    forward substitution, then the off-diagonal blocks level by level,
-//    T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ, spread over all threads.
+//    T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ, as warp-level m16n8k8 MMAs with
+//    both operands split into tf32 hi + lo parts (fp32-level accuracy).
 //  * w and u are two more M = 128 MMAs with A = [T' ; unused rows], reading
 //    k exp2(g2) and v as MN-major B operands in place.
 //  * qg, Aqk, w and u leave through TMA stores from swizzled shared memory;
@@ -58,6 +59,38 @@ __device__ __forceinline__ float bf16_at(const uint8_t* p) {
     return __uint_as_float(((uint32_t)(*(const uint16_t*)p)) << 16);
 }
 
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32_16x8x8(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// d += a * b for one m16n8k8 fragment pair at fp32-level accuracy: both operands
+// are split into tf32 hi + lo parts and the three significant cross products
+// are accumulated (hi*hi into d, hi*lo + lo*hi into c).
+__device__ __forceinline__ void mma3_tf32(float* d, float* c, const float* a, const float* b) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ah[i] = tf32_rna(a[i]);
+        al[i] = tf32_rna(a[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        bh[i] = tf32_rna(b[i]);
+        bl[i] = tf32_rna(b[i] - __uint_as_float(bh[i]));
+    }
+    mma_tf32_16x8x8(d, ah, bh);
+    mma_tf32_16x8x8(c, ah, bl);
+    mma_tf32_16x8x8(c, al, bh);
+}
+
 template <int KB, int VB>
 struct IntraSmem {
     static constexpr int K = 64 * KB, V = 64 * VB;
@@ -67,7 +100,7 @@ struct IntraSmem {
     static constexpr uint32_t KINV_BYTES = 18432;       // >= max(KB*8192, 64*kS*4)
     static constexpr uint32_t VS = KINV + KINV_BYTES;   // v per vb [64][64] SW128; later u staging
     static constexpr uint32_t G = VS + VB * 8192;       // g then g2, fp32 [64][K]; later T fp32 [64][kS] + X
-    static constexpr uint32_t XS = G + 64 * kS * 4;     // X blocks fp32 [3][16][16]
+    static constexpr uint32_t XS = G + 64 * kS * 4;     // per-warp X halves fp32 [6][16][8]
     static constexpr uint32_t G_BYTES = (64 * K * 4 > 64 * kS * 4 + 3 * 1024) ? 64 * K * 4 : 64 * kS * 4 + 3 * 1024;
     static constexpr uint32_t GD = G + G_BYTES;         // G, fp32 [K]
     static constexpr uint32_t EG = GD + K * 4;          // exp2(G), fp32 [K]
@@ -149,14 +182,20 @@ __global__ void __launch_bounds__(256, 2)
 
     // ---- 1. in-chunk cumsum of g (log2 space), two passes of segment sums ---
     const int cd = tid % K, cp = tid / K;  // key dim, segment
-    {
-        float s = 0.f;
+    float gv[R];  // this thread's segment of column cd, loaded once
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int i = cp * R + r;
-            s += (i < valid) ? G[i * K + cd] : 0.f;
+    for (int r = 0; r < R; ++r) gv[r] = G[(cp * R + r) * K + cd];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (cp * R + r >= valid) gv[r] = 0.f;
+    {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; r += 2) {
+            s0 += gv[r];
+            s1 += gv[r + 1];
         }
-        PARTs[cp * K + cd] = s;
+        PARTs[cp * K + cd] = s0 + s1;
     }
     __syncthreads();
     bool unsafe = false;
@@ -166,12 +205,12 @@ __global__ void __launch_bounds__(256, 2)
         float mx = fabsf(acc * kLog2e);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int i = cp * R + r;
-            acc += (i < valid) ? G[i * K + cd] : 0.f;
-            const float g2 = acc * kLog2e;
-            G[i * K + cd] = g2;
-            mx = fmaxf(mx, fabsf(g2));
+            acc += gv[r];
+            gv[r] = acc * kLog2e;
+            mx = fmaxf(mx, fabsf(gv[r]));
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r) G[(cp * R + r) * K + cd] = gv[r];
         if (cp == P - 1) {
             const float Gd = acc * kLog2e;
             GDs[cd] = Gd;
@@ -209,6 +248,7 @@ __global__ void __launch_bounds__(256, 2)
     {
         uint16_t* kg_g = reinterpret_cast<uint16_t*>(ws + L.kg) + tile * 64 * K;
         constexpr int CPR = 8 * KB;  // 16-byte chunks per row
+#pragma unroll 2
         for (int e = tid; e < 64 * CPR; e += 256) {
             const int i = e / CPR, j8 = e % CPR, kb = j8 >> 3, cc = j8 & 7;
             const uint32_t off = i * 128 + ((cc ^ (i & 7)) << 4);
@@ -361,48 +401,51 @@ __global__ void __launch_bounds__(256, 2)
         for (int r = 0; r < 16; ++r) Tsm[(b0 + r) * kS + b0 + cc] = acc[r];
     }
     __syncthreads();
-    // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev
+    // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev.  One warp per
+    // (block, 8-column half): 16x8 outputs by warp-level m16n8k8 MMAs in 3xTF32
+    // (hi/lo split of both operands: fp32-level accuracy), X staged per warp.
+    {
+        const int g = lane >> 2, t = lane & 3;
+        float* xw = Xsm + warp * 128;  // this warp's X half, [16][8] fp32
 #pragma unroll 1
-    for (int lev = 1; lev < 4; ++lev) {
-        const int nblk = 4 - lev;
-        const bool act = tid < nblk * 64;
-        const int J = tid >> 6, I = J + lev, r = (tid & 63) >> 2, c4 = (tid & 3) * 4;
-        if (act) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int Kb = J; Kb < I; ++Kb) {
+        for (int lev = 1; lev < 4; ++lev) {
+            if (warp < 2 * (4 - lev)) {
+                const int J = warp >> 1, nh = warp & 1, I = J + lev;
+                const int n0 = 16 * J + 8 * nh;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, cor[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int Kb = J; Kb < I; ++Kb) {
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = AMT[(16 * Kb + m) * kS + 16 * I + r];
-                    const float4 t = *reinterpret_cast<const float4*>(Tsm + (16 * Kb + m) * kS + 16 * J + c4);
-                    acc.x = fmaf(a, t.x, acc.x);
-                    acc.y = fmaf(a, t.y, acc.y);
-                    acc.z = fmaf(a, t.z, acc.z);
-                    acc.w = fmaf(a, t.w, acc.w);
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int kc = 16 * Kb + 8 * ks;
+                        const float a[4] = {AMT[(kc + t) * kS + 16 * I + g], AMT[(kc + t) * kS + 16 * I + g + 8],
+                                            AMT[(kc + t + 4) * kS + 16 * I + g],
+                                            AMT[(kc + t + 4) * kS + 16 * I + g + 8]};
+                        const float b[2] = {Tsm[(kc + t) * kS + n0 + g], Tsm[(kc + t + 4) * kS + n0 + g]};
+                        mma3_tf32(acc, cor, a, b);
+                    }
                 }
-            }
-            *reinterpret_cast<float4*>(Xsm + J * 256 + r * 16 + c4) = acc;
-        }
-        __syncthreads();
-        if (act) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float* trow = Tsm + (16 * I + r) * kS + 16 * I;
+                xw[g * 8 + 2 * t] = acc[0] + cor[0];
+                xw[g * 8 + 2 * t + 1] = acc[1] + cor[1];
+                xw[(g + 8) * 8 + 2 * t] = acc[2] + cor[2];
+                xw[(g + 8) * 8 + 2 * t + 1] = acc[3] + cor[3];
+                __syncwarp();
+                float d[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m4 = 0; m4 < 16; m4 += 4) {
-                const float4 tv = *reinterpret_cast<const float4*>(trow + m4);
-                const float tt[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 x = *reinterpret_cast<const float4*>(Xsm + J * 256 + (m4 + q) * 16 + c4);
-                    acc.x = fmaf(tt[q], x.x, acc.x);
-                    acc.y = fmaf(tt[q], x.y, acc.y);
-                    acc.z = fmaf(tt[q], x.z, acc.z);
-                    acc.w = fmaf(tt[q], x.w, acc.w);
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int kc = 16 * I + 8 * ks;
+                    const float a[4] = {Tsm[(16 * I + g) * kS + kc + t], Tsm[(16 * I + g + 8) * kS + kc + t],
+                                        Tsm[(16 * I + g) * kS + kc + t + 4], Tsm[(16 * I + g + 8) * kS + kc + t + 4]};
+                    const float b[2] = {xw[(8 * ks + t) * 8 + g], xw[(8 * ks + t + 4) * 8 + g]};
+                    mma3_tf32(d, dc, a, b);
                 }
+                *reinterpret_cast<float2*>(Tsm + (16 * I + g) * kS + n0 + 2 * t) =
+                    make_float2(-(d[0] + dc[0]), -(d[1] + dc[1]));
+                *reinterpret_cast<float2*>(Tsm + (16 * I + g + 8) * kS + n0 + 2 * t) =
+                    make_float2(-(d[2] + dc[2]), -(d[3] + dc[3]));
+                __syncwarp();
             }
-            *reinterpret_cast<float4*>(Tsm + (16 * I + r) * kS + 16 * J + c4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            __syncthreads();
         }
-        __syncthreads();
     }
     // T' = T diag(beta) -> bf16, K-major SW128 [64 i][64 j] (the Aqk store must have read TP)
     if (tid == 0) bulk_wait_read0();
@@ -486,7 +529,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::VS + vb * 8192, vb * 64, trow);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();  // smem must outlive the reads; the writes complete with the grid
     }
     if (warp == 1) {
         tc_fence_after();
