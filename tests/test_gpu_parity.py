@@ -38,6 +38,14 @@ def test_small_shapes_ragged(K, V, T):
     full_check(x, what=f"K={K} V={V} T={T}")
 
 
+@pytest.mark.parametrize("K,V,H", [(128, 128, 80), (64, 64, 80), (64, 128, 80)])
+def test_many_heads_scan_variants(K, V, H):
+    """Enough (sequence, head) units that the scan switches tile shape: a
+    128-wide V tile per head (V = 128) or two 64-wide CTAs per SM (V = 64)."""
+    x = synth.make_inputs(make(B=2, T=130, H=H, K=K, V=V, seed=H + K + V))
+    full_check(x, what=f"many heads K={K} V={V}")
+
+
 def test_no_initial_state_and_no_final_state():
     x = synth.make_inputs(make(B=1, T=300, H=2, h0=False, seed=5))
     full_check(x, what="h0=None")
