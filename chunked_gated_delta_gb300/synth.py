@@ -55,6 +55,9 @@ WORKLOADS = {
     # a quarter of the headline batch: the size profiler captures run on (its
     # inputs, ~0.4 GB, still exceed L2)
     "quarter": Workload("quarter", B=1, T=8192, H=32, K=128, V=128, seed=20261207),
+    # the same token-heads as "quarter" spread over 128 heads: the scan kernel
+    # runs the headline's grid (128 CTAs, 128-wide V tiles) on 32 chunks each
+    "wide": Workload("wide", B=1, T=2048, H=128, K=128, V=128, seed=20261208),
 }
 
 
