@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     load_library,
     make_dims,
     new_workspace,
+    selftest_wait_timeout,
     status,
     status_string,
     workspace_layout,

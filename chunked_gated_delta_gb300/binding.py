@@ -24,7 +24,7 @@ STATUS_NAMES = {
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
-           "kda_fwd_host", "kda_fwd_noalloc")
+           "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout")
 
 
 class KdaError(RuntimeError):
@@ -75,6 +75,7 @@ def load_library(build_if_missing: bool = True):
             "kda_fwd_host_arena_size": (SZ, [D]),
             "kda_fwd_host": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
             "kda_fwd_noalloc": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P]),
+            "kda_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_ulonglong, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -240,3 +241,10 @@ def fwd_noalloc(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, stream=None):
                                         _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(ht),
                                         ctypes.byref(dims), _stream_handle(stream))
     _check(rc, "kda_fwd_noalloc")
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
+    """Run the bounded-wait self-check; returns the status code (6 = timed out as designed)."""
+    import torch
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    return int(load_library().kda_selftest_wait_timeout(_ptr(word), int(limit_ns), _stream_handle(stream)))

@@ -180,6 +180,17 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const fl
  */
 kda_status kda_fwd_status(const void* workspace, void* stream);
 
+/*
+ * Self-check of the kernels' failure path: one CTA waits, for at most
+ * limit_ns nanoseconds (1 .. 2e9), on a pipeline barrier that nothing
+ * releases, using the same bounded wait as the forward's kernels, and records
+ * the expiry in the int32 status word at status_word (device memory, 4-byte
+ * aligned, owned by the caller).  Synchronises `stream` and returns what
+ * kda_fwd_status would: KDA_ERR_TIMEOUT when the wait expired as designed.
+ * The context stays usable afterwards (no trap, no fault).
+ */
+kda_status kda_selftest_wait_timeout(void* status_word, unsigned long long limit_ns, void* stream);
+
 /* Static description of a status code.  Never NULL. */
 const char* kda_status_string(kda_status s);
 

@@ -114,3 +114,8 @@ def test_validation_errors_before_any_launch(lib):
     assert call_fwd(lib, dv, cu=FAKE) == 1                              # packed batch needs B == 1
     dv = kda.make_dims(1, 128, 2, 128, 128, num_seqs=3)
     assert call_fwd(lib, dv, cu=None) == 1                              # num_seqs without cu_seqlens
+    P = ctypes.c_void_p
+    assert lib.kda_selftest_wait_timeout(None, 1000, None) == 1           # no status word
+    assert lib.kda_selftest_wait_timeout(P(FAKE + 2), 1000, None) == 1    # misaligned
+    assert lib.kda_selftest_wait_timeout(P(FAKE), 0, None) == 1           # no limit
+    assert lib.kda_selftest_wait_timeout(P(FAKE), 10**10, None) == 1      # above the kernels' limit

@@ -258,3 +258,17 @@ def test_host_buffer_entry_point_matches_device_entry_point():
         torch.cuda.synchronize()
         assert torch.equal(o, o_dev.cpu())
         assert torch.equal(ht, ht_dev.cpu())
+
+
+def test_bounded_wait_expires_and_context_survives():
+    """A pipeline wait on a barrier nothing releases ends after its limit with
+    KDA_ERR_TIMEOUT; the context then runs a normal forward correctly."""
+    import time
+    import chunked_gated_delta_gb300 as kda
+    t0 = time.time()
+    assert kda.selftest_wait_timeout(2_000_000) == 6  # 2 ms limit
+    assert time.time() - t0 < 5.0
+    x = synth.make_inputs(make(B=1, T=100, H=2, seed=91))
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = oracle_ref(x)
+    assert_within(compare(x, o, ht, o_ref, ht_ref), "after timeout self-check")
