@@ -129,3 +129,97 @@ def chunked_fwd(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, C=64):
             o[a:b, h] = os_
             ht[s, h] = hs
     return o.reshape(B, T, H, V), ht
+
+
+def chunk_bwd_dh(chunks, do, dv_in, dht, scale):
+    """Reverse state scan of the chunked forward for one (sequence, head), fp64.
+
+    The backward companion of :func:`chunk_scan` in kernel-fun
+    ``kda/_kernels/bwd_dhu.py`` (module docstring): with dh the gradient of the
+    loss with respect to the state after the chunk being processed, chunks
+    newest first,
+
+        dhck[c] = dh                                  (checkpoint, before the update)
+        dv2     = kg @ dh + dv_in                     (gradient w.r.t. v' of the chunk)
+        dh      = exp2(G) * dh + scale qg^T @ do - w^T @ dv2
+        dh0     = dh after the oldest chunk
+
+    ``chunks`` from :func:`chunk_intra` (fp64 qg, kg, w, G; qg without scale);
+    do, dv_in: [L, V]; dht: [K, V] (or None = zeros).  Returns (dhck [n_chunks,
+    K, V], dv2 [L, V], dh0 [K, V]).  dv_in carries the chunk-local part of the
+    v' gradient (the Aqk^T do term), which the dh scan takes as an input.
+    """
+    C = chunks[0]["qg"].shape[0] if chunks else 64
+    K = chunks[0]["kg"].shape[1] if chunks else (dht.shape[0] if dht is not None else 0)
+    V = do.shape[1]
+    L = do.shape[0]
+    do_p = _pad_rows(np.asarray(do, np.float64), C)
+    dvi_p = _pad_rows(np.asarray(dv_in, np.float64), C)
+    dh = np.zeros((K, V)) if dht is None else np.array(dht, dtype=np.float64, copy=True)
+    dhck = np.zeros((len(chunks), K, V))
+    dv2 = np.zeros((len(chunks) * C, V))
+    for c in range(len(chunks) - 1, -1, -1):
+        ch = chunks[c]
+        sl = slice(c * C, (c + 1) * C)
+        dhck[c] = dh
+        d2 = ch["kg"] @ dh + dvi_p[sl]
+        d2[ch["valid"]:] = 0.0  # padding rows are not part of the sequence
+        dv2[sl] = d2
+        dh = np.exp2(ch["G"])[:, None] * dh + scale * (ch["qg"].T @ do_p[sl]) - ch["w"].T @ d2
+    return dhck, dv2[:L], dh
+
+
+def scan_with_vprime(chunks, h0, scale, override=None):
+    """The inter-chunk scan with an optional additive perturbation of one
+    chunk's v' (``override = (c, dV)``); returns (o [L, V], ht [K, V]).  Used
+    to check the backward's dv2 by finite differences of the forward."""
+    h = np.array(h0, dtype=np.float64, copy=True)
+    outs = []
+    for c, ch in enumerate(chunks):
+        vp = ch["u"] - ch["w"] @ h
+        if override is not None and override[0] == c:
+            vp = vp + override[1]
+        o = scale * (ch["qg"] @ h) + ch["Aqk"] @ vp
+        h = np.exp2(ch["G"])[:, None] * h + ch["kg"].T @ vp
+        outs.append(o[: ch["valid"]])
+    return np.concatenate(outs, axis=0), h
+
+
+def chunked_bwd_dh(q, k, v, g, beta, scale, do, dv_in, h0=None, dht=None, cu_seqlens=None, C=64):
+    """Reverse state scan over all sequences and heads, fp64 (shapes as the
+    forward; do, dv_in [B,T,H,V]; dht [N,H,K,V] or None).  Returns
+    (dhck [total chunks, H, K, V] in chunk-table order, dv2 [B,T,H,V],
+    dh0 [N,H,K,V])."""
+    q, k, v, g, beta, do, dv_in = (np.asarray(x, np.float64) for x in (q, k, v, g, beta, do, dv_in))
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is None:
+        cu = np.arange(B + 1) * T
+        N = B
+        flat = lambda x: x.reshape((B * T,) + x.shape[2:])  # noqa: E731
+    else:
+        assert B == 1
+        cu = np.asarray(cu_seqlens, np.int64)
+        N = len(cu) - 1
+        flat = lambda x: x[0]  # noqa: E731
+    qf, kf, vf, gf, bf, dof, dvf = (flat(x) for x in (q, k, v, g, beta, do, dv_in))
+    lens = np.diff(cu)
+    tiles = (lens + C - 1) // C
+    base = np.concatenate([[0], np.cumsum(tiles)])
+    dhck = np.zeros((int(base[-1]), H, K, V))
+    dv2 = np.zeros((B * T, H, V))
+    dh0 = np.zeros((N, H, K, V))
+    for s in range(N):
+        a, b = int(cu[s]), int(cu[s + 1])
+        for h in range(H):
+            dhts = None if dht is None else np.asarray(dht, np.float64)[s, h]
+            if b == a:
+                dh0[s, h] = 0.0 if dhts is None else dhts
+                continue
+            chunks = chunk_intra(qf[a:b, h], kf[a:b, h], vf[a:b, h], gf[a:b, h], bf[a:b, h], scale, C)
+            # the scan's qg enters o with scale applied outside; chunk_intra's Aqk has scale inside
+            ck, d2, d0 = chunk_bwd_dh(chunks, dof[a:b, h], dvf[a:b, h], dhts, scale)
+            dhck[base[s]:base[s + 1], h] = ck
+            dv2[a:b, h] = d2
+            dh0[s, h] = d0
+    return dhck, dv2.reshape(B, T, H, V), dh0
