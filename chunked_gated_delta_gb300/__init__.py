@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     EXPORTS,
     Dims,
     KdaError,
+    bwd_dh,
     chunk_table,
     fwd,
     fwd_host,

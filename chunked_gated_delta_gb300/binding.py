@@ -24,7 +24,7 @@ STATUS_NAMES = {
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
-           "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout")
+           "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout", "kda_bwd_dh")
 
 
 class KdaError(RuntimeError):
@@ -76,6 +76,7 @@ def load_library(build_if_missing: bool = True):
             "kda_fwd_host": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
             "kda_fwd_noalloc": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P]),
             "kda_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_ulonglong, P]),
+            "kda_bwd_dh": (ctypes.c_int, [F32, P, P, P, P, P, P, D, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -248,3 +249,29 @@ def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
     import torch
     word = torch.zeros(1, dtype=torch.int32, device="cuda")
     return int(load_library().kda_selftest_wait_timeout(_ptr(word), int(limit_ns), _stream_handle(stream)))
+
+
+def bwd_dh(scale, do, dv_in, dht, dims: Dims, workspace, want_dhck=True, want_dh0=True, stream=None):
+    """Reverse state scan on the GPU (kda_bwd_dh).  ``workspace`` must hold the
+    intra-chunk intermediates of the same inputs (from fwd / fwd_intra).
+    Returns (dhck [max_chunks,H,K,V] bf16 or None, dv2 [B,T,H,V] bf16,
+    dh0 [N,H,K,V] fp32 or None)."""
+    import torch
+    for name, t in (("do", do), ("dv_in", dv_in)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor")
+    if dht is not None and (dht.dtype != torch.float32 or not dht.is_cuda or not dht.is_contiguous()):
+        raise TypeError("dht must be a contiguous CUDA float32 tensor")
+    B, T, H, V = do.shape
+    K = dims.K
+    N = dims.num_seqs if dims.num_seqs > 0 else dims.B
+    lay = workspace_layout(dims)
+    dev = do.device
+    dhck = torch.empty((lay.max_chunks, H, K, V), dtype=torch.bfloat16, device=dev) if want_dhck else None
+    dv2 = torch.zeros((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    dh0 = torch.empty((N, H, K, V), dtype=torch.float32, device=dev) if want_dh0 else None
+    rc = load_library().kda_bwd_dh(float(scale), _ptr(do), _ptr(dv_in), _ptr(dht), _ptr(dhck), _ptr(dv2),
+                                   _ptr(dh0), ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                   _stream_handle(stream))
+    _check(rc, "kda_bwd_dh")
+    return dhck, dv2, dh0

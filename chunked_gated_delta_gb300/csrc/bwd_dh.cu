@@ -1,0 +1,361 @@
+// bwd_dh.cu -- reverse state scan of the chunked KDA forward (sm_103a): the
+// gradient of the loss with respect to the recurrent state, chunk by chunk.
+//
+// One CTA per (sequence, head, V tile of 64*NVB columns), serial over the
+// sequence's chunks, newest first.  With dh the gradient with respect to the
+// state after the chunk (kernel-fun "kda/_kernels/bwd_dhu.py", module
+// docstring; dh starts at dht):
+//
+//   dhck[c] = dh                          (bf16 checkpoint, before the update)
+//   dv2     = kg @ dh + dv_in             (rounded to bf16; gradient w.r.t. v')
+//   dh     <- exp2(G) * dh + scale * qg^T @ do - w^T @ dv2
+//   dh0     = dh after the oldest chunk   (fp32)
+//
+// It reads qg, kg, w and gd from the workspace the intra-chunk kernel wrote
+// for the same inputs, so a training step runs kda_fwd (or kda_fwd_intra)
+// first and keeps its workspace.
+//
+// GB300 mapping (warp-specialised, the forward scan's layout):
+//   warps 0..4*NVB-1   recurrence: thread r owns dh row r (fp32 registers) and,
+//                      in TMEM quadrants 0-1, token row r of dv2.
+//   next warp          TMA producer: kg, qg, w (workspace), do and dv_in (user
+//                      tensors) and gd per chunk into a STAGES-deep ring.
+//   next warp          tcgen05 issuer + TMEM owner.
+// MMAs, all M = 128:
+//   DV = [kg ; qg] @ dh      TMEM lanes 0-63 (rows 64-127 unused)
+//   QD = qg^T @ do           qg read MN-major; 128 lanes = K rows
+//   WD = w^T @ dv2           w read MN-major
+// The chain DV -> dv2 -> WD -> dh -> next DV is issued first; QD overlaps it.
+// Rows of a tail chunk past the sequence end have qg = kg = w = 0 in the
+// workspace, so do there contributes nothing; dv2 rows there are masked.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace kda {
+namespace {
+
+using namespace ptx;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int KB, int NVB, int STAGES>
+struct BwdCfg {
+    static constexpr int K = 64 * KB;
+    static constexpr int BV = 64 * NVB;
+    static constexpr int REC_WARPS = 4 * NVB;
+    static constexpr int TMA_WARP = REC_WARPS;
+    static constexpr int MMA_WARP = REC_WARPS + 1;
+    static constexpr int THREADS = 32 * (REC_WARPS + 2);
+    static constexpr uint32_t TMEM_COLS = NVB == 1 ? 256 : 512;
+    static constexpr int MIN_CTAS = (NVB == 1 && STAGES == 1) ? 2 : 1;
+    // one input stage
+    static constexpr uint32_t AKQ = 0;                     // per kb: [kg 8K | qg 8K]
+    static constexpr uint32_t W = AKQ + 2 * KB * 8192;     // w per kb [64 tok][64 d]
+    static constexpr uint32_t DO = W + KB * 8192;          // do per V block [64 tok][64 v]
+    static constexpr uint32_t DVIN = DO + NVB * 8192;      // dv_in per V block
+    static constexpr uint32_t GD = DVIN + NVB * 8192;      // gd fp32 [K]
+    static constexpr uint32_t STAGE = GD + 1024;
+    static constexpr uint32_t TX_BYTES = (3 * KB + 2 * NVB) * 8192 + K * 4;
+    // persistent
+    static constexpr uint32_t HS = STAGES * STAGE;         // dh bf16 per V block [K rows][64 v], MN-major
+    static constexpr uint32_t HS_BLOCK = KB * 8192;
+    static constexpr uint32_t VP = HS + NVB * HS_BLOCK;    // dv2 bf16 per V block [64 tok][64 v], MN-major
+    static constexpr uint32_t BYTES = VP + NVB * 8192;
+};
+
+template <int STAGES>
+struct BwdBars {
+    uint64_t full[STAGES], empty[STAGES];
+    uint64_t h_ready, dv_full, vp_ready, upd_full;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+template <int KB, int NVB, int STAGES>
+__global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, NVB, STAGES>::MIN_CTAS)
+    kda_bwd_dh_kernel(const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_qg,
+                      const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dvin, const float* __restrict__ dht,
+                      uint16_t* __restrict__ dhck, uint16_t* __restrict__ dv2, float* __restrict__ dh0,
+                      uint8_t* __restrict__ ws, const WsLayout L, const float scale, const int H, const int V) {
+    using S = BwdCfg<KB, NVB, STAGES>;
+    constexpr int K = S::K;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ BwdBars<STAGES> B;
+
+    const int NT = V / S::BV;
+    const int vt = blockIdx.x % NT;
+    const int h = (blockIdx.x / NT) % H;
+    const int s = blockIdx.x / (NT * H);
+    const int v0 = vt * S::BV;
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
+    const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
+    const int tiles = si.tiles;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (tid == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&B.full[i], 1);
+            mbar_init(&B.empty[i], 1 + S::REC_WARPS);
+        }
+        mbar_init(&B.h_ready, S::REC_WARPS);
+        mbar_init(&B.dv_full, 1);
+        mbar_init(&B.vp_ready, 2 * NVB);
+        mbar_init(&B.upd_full, 1);
+        B.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == S::MMA_WARP) {
+        tmem_alloc(&B.tmem_slot, S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B.tmem_slot;
+    const uint32_t t_dv = tmem, t_qd = tmem + S::BV, t_wd = tmem + 2 * S::BV;
+    volatile int* abort_flag = &B.abort_flag;
+    bool timed_out = false;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+        timed_out = true;
+        *abort_flag = 1;
+        return false;
+    };
+
+    if (warp < S::REC_WARPS) {
+        // ================= recurrence warps =================
+        const int quad = warp & 3, vb = warp >> 2;
+        const int r = quad * 32 + lane;  // dh row (key dim) and, for r < 64, token row
+        const bool has_row = r < K;      // warp-uniform
+        const int col = v0 + vb * 64;
+        float dh[64];
+        if (has_row && dht != nullptr) {
+            const float4* src = reinterpret_cast<const float4*>(dht + (((int64_t)s * H + h) * K + r) * V + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 x = src[j];
+                dh[4 * j] = x.x;
+                dh[4 * j + 1] = x.y;
+                dh[4 * j + 2] = x.z;
+                dh[4 * j + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) dh[j] = 0.f;
+        }
+        uint8_t* hs = sm + S::HS + vb * S::HS_BLOCK;
+        uint8_t* vp = sm + S::VP + vb * 8192;
+        for (int it = 0; it < tiles && !*abort_flag; ++it) {
+            const int c = tiles - 1 - it;
+            const int st = it % STAGES;
+            const uint32_t sp = (it / STAGES) & 1;
+            uint8_t* stage = sm + st * S::STAGE;
+            // checkpoint and MMA operand: dh before this chunk's update, bf16
+            if (has_row) {
+                uint4* ck = dhck == nullptr ? nullptr
+                                            : reinterpret_cast<uint4*>(
+                                                  dhck + (((int64_t)(si.tile_base + c) * H + h) * K + r) * V + col);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 x = make_uint4(pack_bf16x2(dh[8 * cc], dh[8 * cc + 1]), pack_bf16x2(dh[8 * cc + 2], dh[8 * cc + 3]),
+                                               pack_bf16x2(dh[8 * cc + 4], dh[8 * cc + 5]), pack_bf16x2(dh[8 * cc + 6], dh[8 * cc + 7]));
+                    *reinterpret_cast<uint4*>(hs + r * 128 + ((cc ^ (r & 7)) << 4)) = x;
+                    if (ck) ck[cc] = x;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.h_ready);
+            if (!wait(&B.full[st], sp)) break;
+            if (quad < 2) {
+                // dv2[r, :] = DV[r, :] + dv_in[r, :], rows past the sequence end = 0
+                if (!wait(&B.dv_full, it & 1)) break;
+                tc_fence_after();
+                const int valid = min(64, si.len - c * 64);
+                const bool row_ok = r < valid;
+                uint4* gdst = reinterpret_cast<uint4*>(dv2 + ((int64_t)(si.bos + c * 64 + r) * H + h) * V + col);
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    float dv[16];
+                    tmem_ld16(t_dv + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, dv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = (c0 >> 3) + hh;
+                        const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
+                        const uint4 iv = *reinterpret_cast<const uint4*>(stage + S::DVIN + vb * 8192 + off);
+                        const uint32_t iw[4] = {iv.x, iv.y, iv.z, iv.w};
+                        uint32_t pw[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            pw[t] = row_ok ? pack_bf16x2(dv[8 * hh + 2 * t] + bf_lo(iw[t]), dv[8 * hh + 2 * t + 1] + bf_hi(iw[t]))
+                                           : 0u;
+                        const uint4 x = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        *reinterpret_cast<uint4*>(vp + off) = x;
+                        if (row_ok) gdst[cc] = x;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.vp_ready);
+            }
+            const float decay = has_row ? ex2(reinterpret_cast<const float*>(stage + S::GD)[r]) : 0.f;
+            if (!wait(&B.upd_full, it & 1)) break;
+            tc_fence_after();
+            if (has_row) {
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    float qd[16], wd[16];
+                    tmem_ld16(t_qd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, qd);
+                    tmem_ld16(t_wd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, wd);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) dh[c0 + t] = fmaf(decay, dh[c0 + t], fmaf(scale, qd[t], -wd[t]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.empty[st]);
+        }
+        if (dh0 != nullptr && has_row && !timed_out && !*abort_flag) {
+            float4* dst = reinterpret_cast<float4*>(dh0 + (((int64_t)s * H + h) * K + r) * V + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
+        }
+    } else if (warp == S::TMA_WARP) {
+        // ================= TMA producer =================
+        if (lane == 0 && tiles > 0) {
+            prefetch_tmap(&tm_kg);
+            prefetch_tmap(&tm_qg);
+            prefetch_tmap(&tm_w);
+            prefetch_tmap(&tm_do);
+            prefetch_tmap(&tm_dvin);
+            const float* gd = reinterpret_cast<const float*>(ws + L.gd);
+            for (int it = 0; it < tiles && !*abort_flag; ++it) {
+                const int c = tiles - 1 - it;
+                const int st = it % STAGES;
+                const uint32_t sp = (it / STAGES) & 1;
+                if (!wait(&B.empty[st], sp ^ 1)) break;
+                uint8_t* stage = sm + st * S::STAGE;
+                const int64_t tile = (int64_t)(si.tile_base + c) * H + h;
+                const int row = (int)(tile * 64);
+                const int trow = si.bos + c * 64;
+                uint64_t* fb = &B.full[st];
+                mbar_arrive_expect_tx(fb, S::TX_BYTES);
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load_2d(stage + S::AKQ + kb * 16384, &tm_kg, fb, kb * 64, row);
+                    tma_load_2d(stage + S::AKQ + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
+                    tma_load_2d(stage + S::W + kb * 8192, &tm_w, fb, kb * 64, row);
+                }
+#pragma unroll
+                for (int vb = 0; vb < NVB; ++vb) {
+                    tma_load_3d(stage + S::DO + vb * 8192, &tm_do, fb, v0 + vb * 64, h, trow);
+                    tma_load_3d(stage + S::DVIN + vb * 8192, &tm_dvin, fb, v0 + vb * 64, h, trow);
+                }
+                bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
+            }
+        }
+    } else if (warp == S::MMA_WARP) {
+        // ================= tcgen05 issuer =================
+        if (lane == 0) {
+            constexpr uint32_t id_dv = idesc_bf16_f32(128, S::BV, 0, 1);  // A K-major, B (dh) MN-major
+            constexpr uint32_t id_up = idesc_bf16_f32(128, S::BV, 1, 1);  // A (qg^T, w^T) MN-major
+            for (int it = 0; it < tiles && !*abort_flag; ++it) {
+                const int st = it % STAGES;
+                const uint32_t sp = (it / STAGES) & 1;
+                const uint32_t stage = sbase + st * S::STAGE;
+                if (!wait(&B.full[st], sp)) break;
+                if (!wait(&B.h_ready, it & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < K / 16; ++ks) {
+                    const int kb = ks >> 2, kk = ks & 3;
+                    mma_bf16(t_dv, smem_desc(stage + S::AKQ + kb * 16384 + kk * 32, 16, 1024),
+                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_dv, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&B.dv_full);
+                // QD = qg^T @ do: the qg blocks sit 16 KB apart (K = 64: the next 8 KB are unused rows)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(t_qd, smem_desc(stage + S::AKQ + 8192 + ks * 2048, KB == 2 ? 16384 : 8192, 1024),
+                             smem_desc(stage + S::DO + ks * 2048, 8192, 1024), id_up, ks > 0 ? 1u : 0u);
+                if (!wait(&B.vp_ready, it & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(t_wd, smem_desc(stage + S::W + ks * 2048, 8192, 1024),
+                             smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_up, ks > 0 ? 1u : 0u);
+                mma_commit(&B.upd_full);
+                mma_commit(&B.empty[st]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == S::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, S::TMEM_COLS);
+    }
+    if (timed_out) atomicOr(status, kStatusTimeout);
+}
+
+template <int KB, int NVB, int STAGES>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+    using S = BwdCfg<KB, NVB, STAGES>;
+    const uint32_t smem = S::BYTES + 1024;
+    auto kern = kda_bwd_dh_kernel<KB, NVB, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = (int64_t)a.N * a.H * (a.V / S::BV);
+    if (ctas <= 0) return cudaSuccess;
+    kern<<<(unsigned)ctas, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.dht,
+                                                       a.dhck, a.dv2, a.dh0, a.ws, a.L, a.scale, a.H, a.V);
+    return cudaGetLastError();
+}
+
+template <int KB>
+cudaError_t launch_bwd_k(const BwdArgs& a, cudaStream_t stream, int sms) {
+    const int64_t ctas64 = (int64_t)a.N * a.H * (a.V / 64);
+    if (ctas64 <= sms) return launch_bwd_t<KB, 1, 2>(a, stream);
+    if (a.V % 128 == 0) return launch_bwd_t<KB, 2, 2>(a, stream);
+    return launch_bwd_t<KB, 1, 1>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    if (a.K == 128) return launch_bwd_k<2>(a, stream, sms);
+    if (a.K == 64) return launch_bwd_k<1>(a, stream, sms);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

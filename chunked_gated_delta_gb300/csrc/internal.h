@@ -30,9 +30,23 @@ struct ScanArgs {
     int N, H, K, V;
 };
 
+struct BwdArgs {
+    CUtensorMap tm_kg, tm_qg, tm_w;  // workspace tiles, 2-D {dim, tiles*64}
+    CUtensorMap tm_do, tm_dvin;      // user tensors, 3-D {V, H, rows}
+    const float* dht;   // [N, H, K, V] or null
+    uint16_t* dhck;     // bf16 [chunks, H, K, V] or null
+    uint16_t* dv2;      // bf16 [rows, H, V]
+    float* dh0;         // [N, H, K, V] or null
+    uint8_t* ws;
+    WsLayout L;
+    float scale;
+    int N, H, K, V;
+};
+
 cudaError_t launch_plan(const int32_t* cu_seqlens, int N, int B, int T, uint8_t* ws,
                         const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_intra(const IntraArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace kda

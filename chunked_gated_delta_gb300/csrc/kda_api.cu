@@ -266,6 +266,48 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
     return KDA_OK;
 }
 
+kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const float* dht, void* dhck, void* dv2,
+                      float* dh0, const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    WsLayout L;
+    st = check_ws(dims, varlen, workspace, workspace_bytes, &L);
+    if (st != KDA_OK) return st;
+    const int64_t rows = (int64_t)dims->B * dims->T;
+    if (rows > 0 && (!do_ || !dv_in || !dv2)) return KDA_ERR_INVALID_ARG;
+    if ((do_ && !aligned(do_, 16)) || (dv_in && !aligned(dv_in, 16)) || (dv2 && !aligned(dv2, 16)) ||
+        (dht && !aligned(dht, 16)) || (dhck && !aligned(dhck, 16)) || (dh0 && !aligned(dh0, 16)))
+        return KDA_ERR_ALIGNMENT;
+    BwdArgs a{};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t trows = L.max_chunks * dims->H * kChunk;
+    if (trows > 0 && rows > 0) {
+        bool ok = map2(&a.tm_kg, ws + L.kg, dims->K, trows);
+        ok = ok && map2(&a.tm_qg, ws + L.qg, dims->K, trows);
+        ok = ok && map2(&a.tm_w, ws + L.w, dims->K, trows);
+        ok = ok && map3(&a.tm_do, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, do_, dims->V, dims->H, rows, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && map3(&a.tm_dvin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv_in, dims->V, dims->H, rows, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return KDA_ERR_CUDA;
+    }
+    a.dht = dht;
+    a.dhck = static_cast<uint16_t*>(dhck);
+    a.dv2 = static_cast<uint16_t*>(dv2);
+    a.dh0 = dh0;
+    a.ws = ws;
+    a.L = L;
+    a.scale = scale;
+    a.N = varlen ? dims->num_seqs : dims->B;
+    a.H = dims->H;
+    a.K = dims->K;
+    a.V = dims->V;
+    if (launch_bwd_dh(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
                    float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
                    const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {

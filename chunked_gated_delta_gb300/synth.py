@@ -109,3 +109,16 @@ def make_inputs(w: Workload, lengths=None, h0=None, dtype_g=torch.float32):
         h0 = 0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32)
     return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=K ** -0.5,
                 B=B, T=T, H=H, K=K, V=V, N=N)
+
+
+def make_bwd_inputs(x: dict, seed: int = 0, dht: bool = True):
+    """Upstream gradients for the reverse state scan of the inputs ``x`` (from
+    :func:`make_inputs`), drawn on the CPU: do and dv_in bf16 [B,T,H,V] with
+    N(0, 1) entries (dv_in stands for the chunk-local Aqk^T do term, of the same
+    magnitude), dht fp32 [N,H,K,V] N(0, 0.1^2) or None."""
+    gen = torch.Generator().manual_seed(1_000_003 + 31 * seed + int(x["T"]))
+    B, T, H, K, V, N = x["B"], x["T"], x["H"], x["K"], x["V"], x["N"]
+    do = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    dv_in = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    dh_t = 0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32) if dht else None
+    return dict(do=do, dv_in=dv_in, dht=dh_t)

@@ -114,6 +114,29 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Reverse state scan (the backward of the inter-chunk stage): the gradient of
+ * the loss with respect to the recurrent state at every chunk boundary, after
+ * kernel-fun "kda/_kernels/bwd_dhu.py".  With dh the gradient w.r.t. the state
+ * after a chunk (starting from dht), chunks newest first:
+ *     dhck[c] = dh;   dv2 = kg @ dh + dv_in;
+ *     dh = exp2(G) * dh + scale * qg^T @ do - w^T @ dv2;   dh0 = final dh.
+ * `workspace` must hold the intra-chunk intermediates of the same inputs and
+ * dims (kda_fwd or kda_fwd_intra run before, workspace kept).
+ *   do        bf16 [B, T, H, V]   gradient of the loss w.r.t. o
+ *   dv_in     bf16 [B, T, H, V]   the chunk-local part of the v' gradient
+ *                                 (the Aqk^T do term), from an earlier stage
+ *   dht       fp32 [N, H, K, V]   gradient w.r.t. the final state, or NULL = 0
+ *   dhck      bf16 [chunks, H, K, V] checkpoints in chunk-table order (chunks =
+ *             kda_workspace_layout().max_chunks), or NULL = not stored
+ *   dv2       bf16 [B, T, H, V]   gradient w.r.t. v' (valid rows written)
+ *   dh0       fp32 [N, H, K, V]   gradient w.r.t. h0, or NULL = not stored
+ * Asynchronous on `stream`; kernel-side errors via kda_fwd_status(workspace).
+ */
+kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const float* dht, void* dhck,
+                      void* dv2, float* dh0, const kda_dims* dims, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * End-to-end forward from HOST buffers.  Copies q, k, v, g, beta (and h0,
  * cu_seqlens when given) from host memory into `arena`, runs kda_fwd there,
  * and copies o (and ht) back to host memory -- one cudaMemcpyAsync per tensor,

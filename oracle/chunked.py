@@ -185,11 +185,13 @@ def scan_with_vprime(chunks, h0, scale, override=None):
     return np.concatenate(outs, axis=0), h
 
 
-def chunked_bwd_dh(q, k, v, g, beta, scale, do, dv_in, h0=None, dht=None, cu_seqlens=None, C=64):
+def chunked_bwd_dh(q, k, v, g, beta, scale, do, dv_in, h0=None, dht=None, cu_seqlens=None, C=64,
+                   units=None):
     """Reverse state scan over all sequences and heads, fp64 (shapes as the
     forward; do, dv_in [B,T,H,V]; dht [N,H,K,V] or None).  Returns
     (dhck [total chunks, H, K, V] in chunk-table order, dv2 [B,T,H,V],
-    dh0 [N,H,K,V])."""
+    dh0 [N,H,K,V]).  ``units`` (a list of (sequence, head)) restricts the work
+    to those units; every other entry of the results is NaN."""
     q, k, v, g, beta, do, dv_in = (np.asarray(x, np.float64) for x in (q, k, v, g, beta, do, dv_in))
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -206,20 +208,21 @@ def chunked_bwd_dh(q, k, v, g, beta, scale, do, dv_in, h0=None, dht=None, cu_seq
     lens = np.diff(cu)
     tiles = (lens + C - 1) // C
     base = np.concatenate([[0], np.cumsum(tiles)])
-    dhck = np.zeros((int(base[-1]), H, K, V))
-    dv2 = np.zeros((B * T, H, V))
-    dh0 = np.zeros((N, H, K, V))
-    for s in range(N):
+    fill = 0.0 if units is None else np.nan
+    dhck = np.full((int(base[-1]), H, K, V), fill)
+    dv2 = np.full((B * T, H, V), fill)
+    dh0 = np.full((N, H, K, V), fill)
+    todo = [(s, h) for s in range(N) for h in range(H)] if units is None else list(units)
+    for s, h in todo:
         a, b = int(cu[s]), int(cu[s + 1])
-        for h in range(H):
-            dhts = None if dht is None else np.asarray(dht, np.float64)[s, h]
-            if b == a:
-                dh0[s, h] = 0.0 if dhts is None else dhts
-                continue
-            chunks = chunk_intra(qf[a:b, h], kf[a:b, h], vf[a:b, h], gf[a:b, h], bf[a:b, h], scale, C)
-            # the scan's qg enters o with scale applied outside; chunk_intra's Aqk has scale inside
-            ck, d2, d0 = chunk_bwd_dh(chunks, dof[a:b, h], dvf[a:b, h], dhts, scale)
-            dhck[base[s]:base[s + 1], h] = ck
-            dv2[a:b, h] = d2
-            dh0[s, h] = d0
+        dhts = None if dht is None else np.asarray(dht, np.float64)[s, h]
+        if b == a:
+            dh0[s, h] = 0.0 if dhts is None else dhts
+            continue
+        chunks = chunk_intra(qf[a:b, h], kf[a:b, h], vf[a:b, h], gf[a:b, h], bf[a:b, h], scale, C)
+        # the scan's qg enters o with scale applied outside; chunk_intra's Aqk has scale inside
+        ck, d2, d0 = chunk_bwd_dh(chunks, dof[a:b, h], dvf[a:b, h], dhts, scale)
+        dhck[base[s]:base[s + 1], h] = ck
+        dv2[a:b, h] = d2
+        dh0[s, h] = d0
     return dhck, dv2.reshape(B, T, H, V), dh0

@@ -119,3 +119,24 @@ def test_validation_errors_before_any_launch(lib):
     assert lib.kda_selftest_wait_timeout(P(FAKE + 2), 1000, None) == 1    # misaligned
     assert lib.kda_selftest_wait_timeout(P(FAKE), 0, None) == 1           # no limit
     assert lib.kda_selftest_wait_timeout(P(FAKE), 10**10, None) == 1      # above the kernels' limit
+
+
+def call_bwd(lib, dims, do=FAKE, dv_in=FAKE, dht=None, dhck=None, dv2=FAKE, dh0=None, ws=FAKE,
+             ws_bytes=1 << 40):
+    P = ctypes.c_void_p
+    return lib.kda_bwd_dh(0.1, P(do), P(dv_in), P(dht), P(dhck), P(dv2), P(dh0),
+                          ctypes.byref(dims) if dims is not None else None, P(ws), ws_bytes, None)
+
+
+def test_bwd_validation_errors_before_any_launch(lib):
+    d = kda.make_dims(1, 128, 2, 128, 128)
+    assert call_bwd(lib, None) == 1                                     # NULL dims
+    assert call_bwd(lib, kda.make_dims(1, 128, 2, 96, 128)) == 2        # K unsupported
+    assert call_bwd(lib, d, ws=0) == 4                                  # no workspace
+    assert call_bwd(lib, d, ws_bytes=1024) == 4                         # too small
+    assert call_bwd(lib, d, do=0) == 1                                  # NULL do
+    assert call_bwd(lib, d, dv_in=0) == 1                               # NULL dv_in
+    assert call_bwd(lib, d, dv2=0) == 1                                 # NULL dv2
+    assert call_bwd(lib, d, do=FAKE + 2) == 3                           # misaligned do
+    assert call_bwd(lib, d, dht=FAKE + 4) == 3                          # misaligned dht
+    assert call_bwd(lib, d, dh0=FAKE + 8) == 3                          # misaligned dh0

@@ -1,0 +1,215 @@
+"""GPU parity of the reverse state scan (kda_bwd_dh) against the fp64 oracle.
+
+The GPU reads qg, kg, w and the chunk decay from the workspace of a forward
+call on the same inputs (bf16 operands, fp32 state), the oracle recomputes
+them in fp64 from the same bf16 inputs.  Tolerances are the forward's: every
+operand of the three products per chunk is rounded to bf16 once (relative
+error 2^-9) and accumulated in fp32, and dv2 is returned in bf16.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_gb300 import synth
+from oracle import chunked as oc
+from parity_util import make, sample_units, to_dev
+
+pytestmark = pytest.mark.gpu
+
+REL = 5e-3      # ||x - x_ref|| / ||x_ref|| for dhck, dv2 and dh0
+MAXREL = 2e-2   # max|x - x_ref| <= MAXREL * max|x_ref|
+
+
+def _dims(x):
+    import chunked_gated_delta_gb300 as kda
+    return kda.make_dims(x["B"], x["T"], x["H"], x["K"], x["V"],
+                         0 if x["cu_seqlens"] is None else x["N"])
+
+
+def run_bwd(x, gr, want_dhck=True, want_dh0=True, workspace=None):
+    """Forward (to fill the workspace), then the reverse state scan."""
+    import chunked_gated_delta_gb300 as kda
+    d, gd = to_dev(x), to_dev(gr)
+    dims = _dims(x)
+    ws = kda.new_workspace(dims, "cuda") if workspace is None else workspace
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+            cu_seqlens=d["cu_seqlens"], output_final_state=False, workspace=ws)
+    out = kda.bwd_dh(x["scale"], gd["do"], gd["dv_in"], gd["dht"], dims, ws,
+                     want_dhck=want_dhck, want_dh0=want_dh0)
+    torch.cuda.synchronize()
+    assert kda.status(ws) == 0
+    return out
+
+
+def oracle_bwd(x, gr, units=None):
+    f = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    return oc.chunked_bwd_dh(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta"]), x["scale"],
+                             f(gr["do"]), f(gr["dv_in"]), dht=f(gr["dht"]),
+                             cu_seqlens=None if x["cu_seqlens"] is None else x["cu_seqlens"].numpy(),
+                             units=units)
+
+
+def _bounds(x):
+    if x["cu_seqlens"] is None:
+        lens = [x["T"]] * x["B"]
+        starts = [b * x["T"] for b in range(x["B"])]
+    else:
+        cu = x["cu_seqlens"].tolist()
+        lens = [cu[s + 1] - cu[s] for s in range(len(cu) - 1)]
+        starts = cu[:-1]
+    tiles = [(n + 63) // 64 for n in lens]
+    base = np.concatenate([[0], np.cumsum(tiles)]).astype(int)
+    return starts, lens, base
+
+
+def _metrics(got, want, what):
+    got, want = np.concatenate(got), np.concatenate(want)
+    if want.size == 0:
+        return {}
+    assert np.all(np.isfinite(got)), f"non-finite values in {what}"
+    nref = np.linalg.norm(want)
+    if nref == 0:
+        return {f"abs_{what}": float(np.max(np.abs(got)))}
+    return {f"rel_{what}": float(np.linalg.norm(got - want) / nref),
+            f"maxrel_{what}": float(np.max(np.abs(got - want)) / np.max(np.abs(want)))}
+
+
+def compare_bwd(x, gpu, ref, units=None):
+    dhck_g, dv2_g, dh0_g = gpu
+    dhck_r, dv2_r, dh0_r = ref
+    H = x["H"]
+    units = units or [(s, h) for s in range(x["N"]) for h in range(H)]
+    starts, lens, base = _bounds(x)
+    dv2_flat_g = dv2_g.float().cpu().numpy().astype(np.float64).reshape(-1, H, x["V"])
+    dv2_flat_r = dv2_r.reshape(-1, H, x["V"])
+    res = {}
+    a, b = [], []
+    for s, h in units:
+        sl = slice(starts[s], starts[s] + lens[s])
+        a.append(dv2_flat_g[sl, h].ravel())
+        b.append(dv2_flat_r[sl, h].ravel())
+    res.update(_metrics(a, b, "dv2"))
+    if dhck_g is not None:
+        ck = dhck_g[: int(base[-1])].float().cpu().numpy().astype(np.float64)  # slots past the table are unused
+        a = [ck[base[s]:base[s + 1], h].ravel() for s, h in units]
+        b = [dhck_r[base[s]:base[s + 1], h].ravel() for s, h in units]
+        res.update(_metrics(a, b, "dhck"))
+    if dh0_g is not None:
+        d0 = dh0_g.cpu().numpy().astype(np.float64)
+        res.update(_metrics([d0[s, h].ravel() for s, h in units], [dh0_r[s, h].ravel() for s, h in units],
+                            "dh0"))
+    return res
+
+
+def assert_bwd_within(res, what=""):
+    assert res, what
+    for key, val in res.items():
+        if key.startswith("rel_"):
+            assert val <= REL, (what, res)
+        elif key.startswith("maxrel_"):
+            assert val <= MAXREL, (what, res)
+        else:
+            assert val <= 1e-6, (what, res)
+
+
+def full_bwd_check(x, gr, what="", **kw):
+    gpu = run_bwd(x, gr, **kw)
+    res = compare_bwd(x, gpu, oracle_bwd(x, gr))
+    assert_bwd_within(res, what)
+    return res
+
+
+# ------------------------------------------------------------------ shapes
+
+def test_tiny_workload():
+    x = synth.make_inputs(synth.WORKLOADS["tiny"])
+    full_bwd_check(x, synth.make_bwd_inputs(x), "tiny")
+
+
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("V", [64, 128])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_small_shapes_ragged(K, V, T):
+    x = synth.make_inputs(make(B=2, T=T, H=2, K=K, V=V, seed=5 + T + K + V))
+    full_bwd_check(x, synth.make_bwd_inputs(x, seed=T), f"K{K} V{V} T{T}")
+
+
+@pytest.mark.parametrize("K,V,H", [(128, 128, 96), (64, 64, 96), (64, 128, 96), (128, 64, 40)])
+def test_many_heads_kernel_variants(K, V, H):
+    """Enough (sequence, head, V tile) units to select the two-V-block and the
+    single-stage kernels as well as the small-grid one."""
+    x = synth.make_inputs(make(B=2, T=130, H=H, K=K, V=V, seed=H + V))
+    full_bwd_check(x, synth.make_bwd_inputs(x), f"K{K} V{V} H{H}")
+
+
+def test_no_dht_and_optional_outputs():
+    x = synth.make_inputs(make(B=2, T=129, H=2, seed=41))
+    gr = synth.make_bwd_inputs(x, dht=False)
+    full_bwd_check(x, gr, "dht None")
+    _, dv2_a, _ = run_bwd(x, gr)
+    dhck, dv2_b, dh0 = run_bwd(x, gr, want_dhck=False, want_dh0=False)
+    assert dhck is None and dh0 is None
+    assert torch.equal(dv2_a, dv2_b)
+
+
+def test_varlen_small_with_empty_and_edge_lengths():
+    lengths = [1, 0, 63, 64, 65, 130, 0, 7]
+    x = synth.make_inputs(make(T=0, H=3, seed=12), lengths=lengths)
+    gr = synth.make_bwd_inputs(x)
+    full_bwd_check(x, gr, "varlen small")
+    _, _, dh0 = run_bwd(x, gr)
+    for s, n in enumerate(lengths):
+        if n == 0:  # no chunk: the gradient passes through unchanged
+            torch.testing.assert_close(dh0[s].cpu(), gr["dht"][s], rtol=0, atol=0)
+
+
+def test_strong_decay():
+    x = synth.make_inputs(make(B=1, T=200, H=2, mu=-6.0, seed=22))
+    full_bwd_check(x, synth.make_bwd_inputs(x), "strong decay")
+
+
+def test_mid_workload_full():
+    x = synth.make_inputs(synth.WORKLOADS["mid"])
+    full_bwd_check(x, synth.make_bwd_inputs(x), "mid")
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+
+def _sampled(name, n, include=()):
+    x = synth.make_inputs(synth.WORKLOADS[name])
+    gr = synth.make_bwd_inputs(x)
+    units = sample_units(x, n, seed=3, include=include)
+    gpu = run_bwd(x, gr)
+    res = compare_bwd(x, gpu, oracle_bwd(x, gr, units=units), units=units)
+    assert_bwd_within(res, name)
+    return x, gr, gpu
+
+
+def test_headline_workload_sampled_and_linear():
+    x, gr, (dhck, dv2, dh0) = _sampled("headline", 4, include=[(0, 0), (3, 31)])
+    # the reverse scan is linear in (do, dv_in, dht): doubling them doubles every
+    # output bit for bit (power-of-two scaling commutes with every rounding)
+    gr2 = {k_: 2 * v_ for k_, v_ in gr.items()}
+    dhck2, dv22, dh02 = run_bwd(x, gr2)
+    assert torch.equal(dhck2, 2 * dhck)
+    assert torch.equal(dv22, 2 * dv2)
+    assert torch.equal(dh02, 2 * dh0)
+
+
+def test_varlen_workload_sampled():
+    _sampled("varlen", 6)
+
+
+def test_long_workload_sampled():
+    _sampled("long", 2, include=[(0, 0)])
+
+
+def test_deterministic():
+    x = synth.make_inputs(make(B=2, T=300, H=4, seed=8))
+    gr = synth.make_bwd_inputs(x)
+    a = run_bwd(x, gr)
+    b = run_bwd(x, gr)
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
