@@ -7,6 +7,10 @@ state), inputs resident in HBM.  The inputs (1.6 GB) are larger than L2, so
 no flush is done between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                  [--path fwd|bwd_dh] [--workload NAME]
+
+--path bwd_dh times the reverse state scan (kda_bwd_dh) instead, on the
+forward's workspace of the same inputs, and prints its own line.
 
 --impl reference times the fp64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload on the host cores.  Under
@@ -185,19 +189,25 @@ def run_reference(args):
     w = synth.WORKLOADS[args.workload]
     x = synth.make_inputs(w)
     cores = host_cores()
+    bwd = args.path == "bwd_dh"
+    gr = synth.make_bwd_inputs(x) if bwd else None
     rates = []
     for i in range(args.warmup + args.steps):
-        r, desc, th, dt = oracle_sample_rate(x, args.ref_seconds, cores)
+        if bwd:
+            r, desc, dt = oracle_bwd_sample_rate(x, gr, args.ref_seconds)
+            th = 1
+        else:
+            r, desc, th, dt = oracle_sample_rate(x, args.ref_seconds, cores)
         if i >= args.warmup:
             rates.append((r, dt))
     value = statistics.median(r for r, _ in rates)
     ms = statistics.median(dt for _, dt in rates) * 1000
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": BWD_METRIC if bwd else METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": workload_config(w, x),
+        "config": {**workload_config(w, x), "path": "bwd_dh"} if bwd else workload_config(w, x),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -286,7 +296,7 @@ def run_gb300(args):
     step_flops = flops_per_token_head(K, V) * th
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world) if args.e2e_steps > 0 else None
+    e2e = run_e2e(args, kda, x, dims, stream, dev, world) if args.e2e_steps > 0 else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -317,27 +327,187 @@ def run_gb300(args):
     return 0
 
 
-def run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world):
+BWD_METRIC = "KDA reverse state scan (dh, dv2, dh0) tokens/s (B=4,H=32,T=8192,K=V=128 bf16); % of HBM roofline"
+
+
+def bwd_bytes_per_token_head(K, V, C=64):
+    """Algorithmic HBM bytes per token-head of the reverse state scan: reads qg,
+    kg, w (workspace), do, dv_in and the chunk decay; writes dv2 and the bf16
+    dh checkpoint (K x V per chunk)."""
+    return 3 * K * 2 + 2 * V * 2 + K * 4 / C + V * 2 + K * V * 2 / C
+
+
+def oracle_bwd_sample_rate(x, gr, seconds):
+    """Time the fp64 reverse-scan oracle on a bounded sample of (sequence, head)
+    units (one thread: it is numpy); returns (tokens/s scaled, description, dt)."""
+    from oracle import chunked as oc
+    f = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    B, T, H = x["B"], x["T"], x["H"]
+    sl = lambda t: None if t is None else t[:1]  # noqa: E731
+    args = [f(sl(x[n])) for n in ("q", "k", "v", "g", "beta")]
+    do, dvi = f(sl(gr["do"])), f(sl(gr["dv_in"]))
+    dht = None if gr["dht"] is None else f(gr["dht"][:1])
+    t0 = time.perf_counter()
+    oc.chunked_bwd_dh(*args, x["scale"], do, dvi, dht=dht, units=[(0, 0)])
+    t1 = time.perf_counter() - t0
+    nh = int(max(1, min(H, round(seconds / max(t1, 1e-6)))))
+    t0 = time.perf_counter()
+    oc.chunked_bwd_dh(*args, x["scale"], do, dvi, dht=dht, units=[(0, h) for h in range(nh)])
+    dt = time.perf_counter() - t0
+    desc = (f"fp64 chunked reverse-scan oracle (numpy, 1 thread) on {nh} of the {B * H} (sequence, head) "
+            f"units (sequence 0, heads 0..{nh - 1}), {T} tokens each; rate scaled to whole {H}-head tokens")
+    return T * nh / H / dt, desc, dt
+
+
+def run_gb300_bwd(args):
+    """The reverse state scan (kda_bwd_dh) on the workload: a step is one call
+    over all (sequence, head) units, the forward's workspace already filled."""
+    import torch
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    import chunked_gated_delta_gb300 as kda
+    from chunked_gated_delta_gb300 import synth
+    kda.load_library(build_if_missing=True)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    gr = synth.make_bwd_inputs(x)
+    B, T, H, K, V, N = x["B"], x["T"], x["H"], x["K"], x["V"], x["N"]
+    d = {n: (x[n].to(dev) if isinstance(x[n], torch.Tensor) else x[n]) for n in x}
+    g = {n: (t.to(dev) if t is not None else None) for n, t in gr.items()}
+    dims = kda.make_dims(B, T, H, K, V, 0 if x["cu_seqlens"] is None else N)
+    ws = kda.new_workspace(dims, dev)
+    stream = torch.cuda.current_stream(dev)
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+            output_final_state=False, workspace=ws, stream=stream)
+    lay = kda.workspace_layout(dims)
+    dhck = torch.empty((lay.max_chunks, H, K, V), dtype=torch.bfloat16, device=dev)
+    dv2 = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    dh0 = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+    lib = kda.load_library()
+    import ctypes
+    P = lambda t: ctypes.c_void_p(0 if t is None else t.data_ptr())  # noqa: E731
+
+    def step():
+        rc = lib.kda_bwd_dh(ctypes.c_float(x["scale"]), P(g["do"]), P(g["dv_in"]), P(g["dht"]), P(dhck),
+                            P(dv2), P(dh0), ctypes.byref(dims), P(ws), ws.numel(),
+                            ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(kda.status_string(rc))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if kda.status(ws, stream) != 0:
+        raise RuntimeError("kernel status")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms_per_step = max_over_ranks(ev[0].elapsed_time(ev[-1]) / args.steps, world)
+    tokens = B * T if x["cu_seqlens"] is None else int(x["cu_seqlens"][-1])
+    value = tokens * world / (ms_per_step / 1e3)
+    hbm, _, _, peak_kind = peaks()
+    th = tokens * H
+    state = N * H * K * V * 4 * (2 if gr["dht"] is not None else 1)
+    by = bwd_bytes_per_token_head(K, V) * th + state
+    avg = statistics.mean(per)
+    achieved = by / (avg / 1e3) / 1e9
+    traffic = ncu_traffic("kda_bwd_dh_kernel", os.path.join(ROOT, "chunked_gated_delta_gb300", "csrc",
+                                                            "bwd_dh.cu"), w.name)
+
+    # end to end through the public API: upstream gradients from pinned host
+    # memory, dv2 and dh0 back to pinned host memory (dhck stays on the device
+    # for the next backward stage)
+    e2e = None
+    if args.e2e_steps > 0:
+        hin = {n: (t.pin_memory() if t is not None else None) for n, t in gr.items()}
+        dv2_h = torch.empty(dv2.shape, dtype=dv2.dtype, pin_memory=True)
+        dh0_h = torch.empty(dh0.shape, dtype=dh0.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in hin.values() if t is not None)
+        d2h = dv2_h.numel() * 2 + dh0_h.numel() * 4
+
+        def one():
+            for n, t in hin.items():
+                if t is not None:
+                    g[n].copy_(t, non_blocking=True)
+            step()
+            dv2_h.copy_(dv2, non_blocking=True)
+            dh0_h.copy_(dh0, non_blocking=True)
+
+        one()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = max(1, min(args.steps, args.e2e_steps))
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+        e2e = {"value": tokens * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+               "path": "pinned host -> device (do, dv_in, dht), kda_bwd_dh, device -> pinned host (dv2, dh0)"}
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; forward workload inputs plus N(0,1) upstream gradients)",
+        "config": {**workload_config(w, x), "path": "bwd_dh"},
+        "roofline": {"bound": "hbm", "kernel": "kda_bwd_dh_kernel", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": by, "avg_launch_ms": avg},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        r, desc, _ = oracle_bwd_sample_rate(x, gr, args.ref_seconds)
+        line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, kda, x, dims, stream, dev, world):
+    """Same metric end to end through the host-buffer C-ABI call (kda_fwd_host):
+    inputs in pinned host memory, outputs back to pinned host memory, all
+    copies inside the timed region."""
     import torch
     names = ("q", "k", "v", "g", "beta")
     host_in = {n: x[n].pin_memory() for n in names}
     h0_host = x["h0"].pin_memory() if x["h0"] is not None else None
-    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    ht_host = torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True)
+    cu_host = x["cu_seqlens"]
+    B, T, H, K, V, N = x["B"], x["T"], x["H"], x["K"], x["V"], x["N"]
+    o_host = torch.empty((B, T, H, V), dtype=torch.bfloat16, pin_memory=True)
+    ht_host = torch.empty((N, H, K, V), dtype=torch.float32, pin_memory=True)
+    arena = torch.empty(kda.host_arena_size(dims), dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     h2d += 0 if h0_host is None else h0_host.numel() * 4
+    h2d += 0 if cu_host is None else cu_host.numel() * 4
     d2h = o_host.numel() * 2 + ht_host.numel() * 4
     steps = max(1, min(args.steps, args.e2e_steps))
 
     def one():
-        for n in names:
-            d[n].copy_(host_in[n], non_blocking=True)
-        if h0_host is not None:
-            d["h0"].copy_(h0_host, non_blocking=True)
-        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
-                cu_seqlens=d["cu_seqlens"], workspace=ws, out=o, final_state=ht)
-        o_host.copy_(o, non_blocking=True)
-        ht_host.copy_(ht, non_blocking=True)
+        kda.fwd_host(host_in["q"], host_in["k"], host_in["v"], host_in["g"], host_in["beta"], x["scale"],
+                     h0_host, cu_host, o_host, ht_host, dims, arena, stream)
 
     one()
     torch.cuda.synchronize(dev)
@@ -349,9 +519,11 @@ def run_e2e(args, kda, x, d, dims, ws, o, ht, stream, dev, world):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
-    return {"value": x["B"] * x["T"] * world / (ms / 1e3), "unit": "tokens/s",
+    del arena
+    return {"value": B * T * world / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "steps": steps, "path": "pinned host -> device copies, kda_fwd, device -> pinned host"}
+            "steps": steps, "path": "kda_fwd_host: pinned host -> device copies, both kernels, "
+                                    "device -> pinned host, one C-ABI call per step"}
 
 
 def main():
@@ -365,10 +537,14 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=2.0,
                     help="target wall seconds of one bounded oracle sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--path", choices=("fwd", "bwd_dh"), default="fwd",
+                    help="fwd: the forward (default); bwd_dh: the reverse state scan")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    return run_reference(args) if args.impl == "reference" else run_gb300(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300_bwd(args) if args.path == "bwd_dh" else run_gb300(args)
 
 
 if __name__ == "__main__":
