@@ -8,6 +8,7 @@ does not load the library (that happens on the first call).
 from .binding import (  # noqa: F401
     EXPORTS,
     Dims,
+    FwdOpts,
     KdaError,
     bwd_dh,
     chunk_table,

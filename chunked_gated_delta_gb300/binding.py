@@ -24,7 +24,8 @@ STATUS_NAMES = {
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
-           "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout", "kda_bwd_dh")
+           "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout", "kda_bwd_dh",
+           "kda_fwd_ex", "kda_fwd_intra_ex", "kda_fwd_scan_ex")
 
 
 class KdaError(RuntimeError):
@@ -37,6 +38,16 @@ class KdaError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("num_seqs", ctypes.c_int32)]
+
+
+class FwdOpts(ctypes.Structure):
+    """kda_fwd_opts: interface variants of the forward (all zero = kda_fwd)."""
+    _fields_ = [("io_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+                ("beta_logits", ctypes.c_int32), ("qk_heads", ctypes.c_int32)]
+
+
+IO_BF16, IO_F16 = 0, 1
+STATE_F32, STATE_BF16 = 0, 1
 
 
 class WsLayout(ctypes.Structure):
@@ -63,6 +74,7 @@ def load_library(build_if_missing: bool = True):
         lib = ctypes.CDLL(path)
         P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
         D = ctypes.POINTER(Dims)
+        O = ctypes.POINTER(FwdOpts)
         sig = {
             "kda_fwd_workspace_size": (SZ, [D]),
             "kda_fwd": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P, SZ, P]),
@@ -77,6 +89,9 @@ def load_library(build_if_missing: bool = True):
             "kda_fwd_noalloc": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, P]),
             "kda_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_ulonglong, P]),
             "kda_bwd_dh": (ctypes.c_int, [F32, P, P, P, P, P, P, D, P, SZ, P]),
+            "kda_fwd_ex": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, O, P, SZ, P]),
+            "kda_fwd_intra_ex": (ctypes.c_int, [P, P, P, P, P, P, D, O, P, SZ, P]),
+            "kda_fwd_scan_ex": (ctypes.c_int, [F32, P, P, P, D, O, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -139,20 +154,23 @@ def _check(rc, where):
 
 
 def _dims_of(q, v, cu_seqlens):
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     return make_dims(B, T, H, K, V, N), (B if cu_seqlens is None else N)
 
 
 def _check_inputs(q, k, v, g, beta, h0, cu_seqlens):
     import torch
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("g", g, torch.float32), ("beta", beta, torch.bfloat16)):
+    io = q.dtype if q.dtype in (torch.bfloat16, torch.float16) else torch.bfloat16
+    for name, t, dt in (("q", q, io), ("k", k, io), ("v", v, io), ("g", g, torch.float32), ("beta", beta, io)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {dt}")
-    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_cuda or not h0.is_contiguous()):
-        raise TypeError("h0 must be a contiguous CUDA float32 tensor")
+    if k.shape != q.shape:
+        raise TypeError("q and k must have the same shape")
+    if h0 is not None and (h0.dtype not in (torch.float32, torch.bfloat16) or not h0.is_cuda
+                           or not h0.is_contiguous()):
+        raise TypeError("h0 must be a contiguous CUDA float32 or bfloat16 tensor")
     if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda):
         raise TypeError("cu_seqlens must be a CUDA int32 tensor")
 
@@ -166,33 +184,44 @@ def new_workspace(dims: Dims, device):
 
 
 def fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_state=True,
-        workspace=None, out=None, final_state=None, stream=None):
+        workspace=None, out=None, final_state=None, stream=None, beta_logits=False, state_dtype=None):
     """KDA chunked forward on the GPU.  Returns (o, ht) (ht None if not requested).
 
-    q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32 [B,T,H,K] (natural-log decay);
-    beta: bf16 [B,T,H]; h0: fp32 [N,H,K,V] or None; cu_seqlens: int32 [N+1] on the
-    device (B must be 1) or None.  ``workspace`` (uint8 CUDA tensor) may be passed
-    to avoid an allocation per call.
+    q, k: [B,T,Hqk,K]; v: [B,T,H,V]; beta: [B,T,H], all bf16 or all fp16 (o
+    follows); g: fp32 [B,T,H,K] (natural-log decay); h0: [N,H,K,V] fp32 or bf16
+    or None; cu_seqlens: int32 [N+1] on the device (B must be 1) or None.
+    H must be a multiple of Hqk (grouped value heads: value head h reads q/k
+    head h // (H // Hqk)).  ``beta_logits``: beta holds logits, the kernel
+    applies the sigmoid.  ``state_dtype`` (torch.float32 / torch.bfloat16) of ht;
+    defaults to h0's dtype, else fp32.  ``workspace`` (uint8 CUDA tensor) may be
+    passed to avoid an allocation per call.
     """
     import torch
     _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
     lib = load_library()
     dims, N = _dims_of(q, v, cu_seqlens)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hqk, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     if scale is None:
         scale = K ** -0.5
+    if state_dtype is None:
+        state_dtype = h0.dtype if h0 is not None else torch.float32
+    if h0 is not None and h0.dtype != state_dtype:
+        raise TypeError("h0 and ht must have the same dtype")
+    opts = FwdOpts(IO_F16 if q.dtype == torch.float16 else IO_BF16,
+                   STATE_BF16 if state_dtype == torch.bfloat16 else STATE_F32,
+                   1 if beta_logits else 0, Hqk if Hqk != H else 0)
     if workspace is None:
         workspace = new_workspace(dims, q.device)
-    o = out if out is not None else torch.empty((B, T, H, V), dtype=torch.bfloat16, device=q.device)
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
     ht = None
     if output_final_state:
-        ht = final_state if final_state is not None else torch.empty((N, H, K, V), dtype=torch.float32,
+        ht = final_state if final_state is not None else torch.empty((N, H, K, V), dtype=state_dtype,
                                                                       device=q.device)
-    rc = lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
-                     _ptr(cu_seqlens), _ptr(o), _ptr(ht), ctypes.byref(dims), _ptr(workspace),
-                     workspace.numel(), _stream_handle(stream))
-    _check(rc, "kda_fwd")
+    rc = lib.kda_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
+                        _ptr(cu_seqlens), _ptr(o), _ptr(ht), ctypes.byref(dims), ctypes.byref(opts),
+                        _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "kda_fwd_ex")
     return o, ht
 
 
@@ -235,7 +264,10 @@ def fwd_noalloc(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, stream=None):
     """kda_fwd_noalloc: the forward with the library's built-in scratch array as
     workspace (no device allocation by the library).  All tensors are CUDA
     tensors allocated by the caller; o and ht are written in place."""
+    import torch
     _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
+    if q.dtype != torch.bfloat16 or q.shape[2] != v.shape[2] or (h0 is not None and h0.dtype != torch.float32):
+        raise TypeError("kda_fwd_noalloc takes the default interface (bf16 I/O, fp32 state, equal heads)")
     dims, _ = _dims_of(q, v, cu_seqlens)
     scale = q.shape[-1] ** -0.5 if scale is None else scale
     rc = load_library().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),

@@ -12,22 +12,30 @@ namespace kda {
 struct IntraArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_g;      // user inputs, 3-D {dim, H, rows}
     CUtensorMap st_qg, st_w, st_u, st_aqk;   // workspace tiles (stores), 2-D {dim, tiles*64}
-    const uint16_t* beta;                // bf16 bits [rows, H]
+    const uint16_t* beta;                // bf16 or fp16 bits [rows, H]
     uint8_t* ws;
     WsLayout L;
-    int H, K, V;
+    int H, K, V;                         // H = value heads
     int64_t max_chunks;
+    int f16;                             // q, k, v, beta are fp16 (else bf16)
+    int flags;                           // kIntraBetaLogits
+    int group;                           // value heads per q/k head
 };
+
+constexpr int kIntraBetaLogits = 1;
+constexpr int kScanOutF16 = 1;     // o is fp16 (else bf16)
+constexpr int kScanStateBF16 = 2;  // h0 / ht are bf16 (else fp32)
 
 struct ScanArgs {
     CUtensorMap tm_w, tm_qg, tm_kg, tm_u, tm_aqk;  // workspace tiles, 2-D {dim, tiles*64}
-    const float* h0;  // [N, H, K, V] or null
-    float* ht;        // [N, H, K, V] or null
-    uint16_t* o;      // bf16 bits [rows, H, V]
+    const void* h0;   // fp32 (or bf16) [N, H, K, V] or null
+    void* ht;         // fp32 (or bf16) [N, H, K, V] or null
+    uint16_t* o;      // bf16 (or fp16) bits [rows, H, V]
     uint8_t* ws;
     WsLayout L;
     float scale;
     int N, H, K, V;
+    int flags;        // kScanOutF16 | kScanStateBF16
 };
 
 struct BwdArgs {

@@ -48,6 +48,7 @@
 //    them, T' takes the A^T region, and the w / u staging take the T and v
 //    regions.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -71,6 +72,23 @@ __device__ __forceinline__ float bf16_at(const uint8_t* p) {
     return __uint_as_float(((uint32_t)(*(const uint16_t*)p)) << 16);
 }
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// Inputs q, k, v, beta are bf16 or (F16) fp16; everything computed on chip and
+// every intermediate written to the workspace is bf16.
+template <bool F16>
+__device__ __forceinline__ float in_lo(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+    else return bf_lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float in_hi(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    else return bf_hi(w);
+}
+template <bool F16>
+__device__ __forceinline__ float in_at(const uint8_t* p) {
+    return in_lo<F16>((uint32_t)(*(const uint16_t*)p));
+}
 
 __device__ __forceinline__ uint32_t tf32_rna(float x) {
     uint32_t r;
@@ -112,7 +130,7 @@ struct Mat64 {
 // fp32 [64][K].  Writes Aqk (bf16, zero above the diagonal) to global memory
 // and beta_i * (k_i . k_j gated) for j < i into A^T, after every thread has
 // finished reading g2s (which A^T overwrites).
-template <int K>
+template <int K, bool F16>
 __device__ __noinline__ void exact_gated_sums(const uint8_t* qk, float* g2s, const float* beta_s, int valid,
                                               uint16_t* aqk_g, Mat64 AMT) {
     constexpr int kPairs = 64 * 64 / kThreads;
@@ -124,9 +142,9 @@ __device__ __noinline__ void exact_gated_sums(const uint8_t* qk, float* g2s, con
         if (j <= i && i < valid) {
             for (int d = 0; d < K; ++d) {
                 const uint8_t* qb = qk + (d >> 6) * 16384;
-                const float qi = bf16_at(qb + sw128_offset(i, d & 63));
-                const float ki = bf16_at(qb + 8192 + sw128_offset(i, d & 63));
-                const float kj = bf16_at(qb + 8192 + sw128_offset(j, d & 63));
+                const float qi = in_at<F16>(qb + sw128_offset(i, d & 63));
+                const float ki = in_at<F16>(qb + 8192 + sw128_offset(i, d & 63));
+                const float kj = in_at<F16>(qb + 8192 + sw128_offset(j, d & 63));
                 const float gate = ex2(g2s[i * K + d] - g2s[j * K + d]);
                 a = fmaf(qi * kj, gate, a);
                 b = fmaf(ki * kj, gate, b);
@@ -169,13 +187,15 @@ struct IntraSmem {
     static_assert(NSEG * K * 4 == 4096, "segment sums are 4 KB");
 };
 
-template <int KB, int VB>
+// flags: kIntraBetaLogits = beta holds logits (sigmoid applied here).
+// group: value heads per q/k head (value head h reads q/k head h / group).
+template <int KB, int VB, bool F16>
 __global__ void __launch_bounds__(kThreads, 3)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap st_qg, const __grid_constant__ CUtensorMap st_w,
                      const __grid_constant__ CUtensorMap st_u, const uint16_t* __restrict__ beta,
-                     uint8_t* __restrict__ ws, const WsLayout L, const int H) {
+                     uint8_t* __restrict__ ws, const WsLayout L, const int H, const int flags, const int group) {
     using S = IntraSmem<KB, VB>;
     constexpr int K = S::K, V = S::V, NCG = S::NCG, NSEG = S::NSEG, RS = S::RS;
     extern __shared__ uint8_t smem_raw[];
@@ -211,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         mbar_arrive_expect_tx(&bar_qk, S::QK_TX);
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) {
-            tma_load_3d(sm + S::QK + kb * 16384, &tm_q, &bar_qk, kb * 64, h, row0);
-            tma_load_3d(sm + S::QK + kb * 16384 + 8192, &tm_k, &bar_qk, kb * 64, h, row0);
+            tma_load_3d(sm + S::QK + kb * 16384, &tm_q, &bar_qk, kb * 64, h / group, row0);
+            tma_load_3d(sm + S::QK + kb * 16384 + 8192, &tm_k, &bar_qk, kb * 64, h / group, row0);
         }
     }
     if (warp == 0) {
@@ -222,7 +242,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (tid >= 64 && tid < 128) {
         const int i = tid - 64;
         float b = 0.f;
-        if (i < valid) b = __uint_as_float(((uint32_t)beta[(int64_t)(row0 + i) * H + h]) << 16);
+        if (i < valid) {
+            b = in_lo<F16>((uint32_t)beta[(int64_t)(row0 + i) * H + h]);
+            if (flags & kIntraBetaLogits) b = 1.f / (1.f + ex2(-b * kLog2e));  // sigmoid
+        }
         beta_s[i] = b;
     }
     tc_fence_before();
@@ -314,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             *reinterpret_cast<float4*>(g2s + (seg * RS + r) * K + d0) =
                 make_float4(gv[r][0], gv[r][1], gv[r][2], gv[r][3]);
         __syncthreads();
-        exact_gated_sums<K>(sm + S::QK, g2s, beta_s, valid, aqk_g, AMT);
+        exact_gated_sums<K, F16>(sm + S::QK, g2s, beta_s, valid, aqk_g, AMT);
     }
     // v into its slot of the g region (free now); it is needed only by the u MMA
     if (tid == 0) {
@@ -334,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             uint2 qv = *reinterpret_cast<const uint2*>(qs + off);
             uint2 kv = *reinterpret_cast<const uint2*>(qs + 8192 + off);
             if (i >= valid) qv = kv = make_uint2(0u, 0u);
-            const float q4[4] = {bf_lo(qv.x), bf_hi(qv.x), bf_lo(qv.y), bf_hi(qv.y)};
-            const float k4[4] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y)};
+            const float q4[4] = {in_lo<F16>(qv.x), in_hi<F16>(qv.x), in_lo<F16>(qv.y), in_hi<F16>(qv.y)};
+            const float k4[4] = {in_lo<F16>(kv.x), in_hi<F16>(kv.x), in_lo<F16>(kv.y), in_hi<F16>(kv.y)};
             float qg4[4], kga4[4], kin4[4], kg4[4];
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -516,9 +539,28 @@ __global__ void __launch_bounds__(kThreads, 3)
     // ---- 5. w^T = (k exp2(g2))^T T'^T, u^T = v^T T'^T  (M = 128 = key / value dims)
     if (warp == 0 && !mbar_wait(&bar_v, 0, kWaitLimitNs)) timed_out = true;
     __syncthreads();
-    for (int e = tid; e < (64 - valid) * 8 * VB; e += kThreads) {  // zero v rows past the end
-        const int rr = valid + e / (8 * VB), x = e % (8 * VB);
-        *reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * 8192 + rr * 128 + (x & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (F16) {
+        // fp16 v -> bf16 in place (the u MMA pairs it with the bf16 T'); rows
+        // past the end -> 0
+        for (int e = tid; e < 64 * 8 * VB; e += kThreads) {
+            const int rr = e / (8 * VB), x = e % (8 * VB);
+            uint4* p = reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * 8192 + rr * 128 + (x & 7) * 16);
+            uint4 y = make_uint4(0u, 0u, 0u, 0u);
+            if (rr < valid) {
+                const uint4 hv = *p;
+                y = make_uint4(pack_bf16x2(in_lo<true>(hv.x), in_hi<true>(hv.x)),
+                               pack_bf16x2(in_lo<true>(hv.y), in_hi<true>(hv.y)),
+                               pack_bf16x2(in_lo<true>(hv.z), in_hi<true>(hv.z)),
+                               pack_bf16x2(in_lo<true>(hv.w), in_hi<true>(hv.w)));
+            }
+            *p = y;
+        }
+    } else {
+        for (int e = tid; e < (64 - valid) * 8 * VB; e += kThreads) {  // zero v rows past the end
+            const int rr = valid + e / (8 * VB), x = e % (8 * VB);
+            *reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * 8192 + rr * 128 + (x & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -586,29 +628,35 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (timed_out) atomicOr(status, kStatusTimeout);
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool F16>
 cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     using S = IntraSmem<KB, VB>;
     const uint32_t smem = S::BYTES + 1024;
-    auto kern = kda_intra_kernel<KB, VB>;
+    auto kern = kda_intra_kernel<KB, VB, F16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t ctas = a.max_chunks * a.H;
     if (ctas <= 0) return cudaSuccess;
     kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_g, a.st_qg, a.st_w, a.st_u,
-                                                     a.beta, a.ws, a.L, a.H);
+                                                     a.beta, a.ws, a.L, a.H, a.flags, a.group);
     return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t launch_intra_d(const IntraArgs& a, cudaStream_t stream) {
+    const int KB = a.K / 64, VB = a.V / 64;
+    if (KB == 2 && VB == 2) return launch_intra_t<2, 2, F16>(a, stream);
+    if (KB == 2 && VB == 1) return launch_intra_t<2, 1, F16>(a, stream);
+    if (KB == 1 && VB == 2) return launch_intra_t<1, 2, F16>(a, stream);
+    if (KB == 1 && VB == 1) return launch_intra_t<1, 1, F16>(a, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_intra(const IntraArgs& a, cudaStream_t stream) {
-    const int KB = a.K / 64, VB = a.V / 64;
-    if (KB == 2 && VB == 2) return launch_intra_t<2, 2>(a, stream);
-    if (KB == 2 && VB == 1) return launch_intra_t<2, 1>(a, stream);
-    if (KB == 1 && VB == 2) return launch_intra_t<1, 2>(a, stream);
-    if (KB == 1 && VB == 1) return launch_intra_t<1, 1>(a, stream);
-    return cudaErrorInvalidValue;
+    if (a.group < 1 || a.H % a.group != 0) return cudaErrorInvalidValue;
+    return a.f16 ? launch_intra_d<true>(a, stream) : launch_intra_d<false>(a, stream);
 }
 
 }  // namespace kda

@@ -118,6 +118,15 @@ bool map3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, i
     return make_tensormap(m, dt, 3, base, dims, strides, box, sw);
 }
 
+bool check_opts(const kda_fwd_opts* op, const kda_dims* d) {
+    if (op->io_dtype != KDA_IO_BF16 && op->io_dtype != KDA_IO_F16) return false;
+    if (op->state_dtype != KDA_STATE_F32 && op->state_dtype != KDA_STATE_BF16) return false;
+    if (op->beta_logits != 0 && op->beta_logits != 1) return false;
+    if (op->qk_heads < 0) return false;
+    if (op->qk_heads > 0 && (op->qk_heads > d->H || d->H % op->qk_heads != 0)) return false;
+    return true;
+}
+
 bool map2(CUtensorMap* m, const void* base, int inner, int64_t rows) {
     const uint64_t dims[2] = {(uint64_t)inner, (uint64_t)rows};
     const uint64_t strides[1] = {(uint64_t)inner * 2};
@@ -177,10 +186,14 @@ int32_t kda_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int32_t chu
     return (int32_t)base;
 }
 
-kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const float* g,
-                         const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+kda_status kda_fwd_intra_ex(const void* q, const void* k, const void* v, const float* g,
+                            const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
+                            const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes,
+                            void* stream) {
     if (!dims) return KDA_ERR_INVALID_ARG;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    if (!check_opts(&op, dims)) return KDA_ERR_INVALID_ARG;
     const bool varlen = is_varlen(dims);
     if (varlen != (cu_seqlens != nullptr)) return KDA_ERR_INVALID_ARG;
     kda_status st = check_dims(dims, varlen);
@@ -202,12 +215,12 @@ kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const floa
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     if (rows == 0 || L.max_chunks == 0) return KDA_OK;
     IntraArgs a{};
-    bool ok = map3(&a.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims->K, dims->H, rows, 64,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && map3(&a.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, dims->K, dims->H, rows, 64,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && map3(&a.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v, dims->V, dims->H, rows, 64,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+    const CUtensorMapDataType io =
+        op.io_dtype == KDA_IO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int hqk = op.qk_heads > 0 ? op.qk_heads : dims->H;
+    bool ok = map3(&a.tm_q, io, 2, q, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a.tm_k, io, 2, k, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a.tm_v, io, 2, v, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && map3(&a.tm_g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g, dims->K, dims->H, rows,
                     (uint32_t)dims->K, CU_TENSOR_MAP_SWIZZLE_NONE);
     const int64_t trows = L.max_chunks * dims->H * kChunk;
@@ -223,13 +236,26 @@ kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const floa
     a.K = dims->K;
     a.V = dims->V;
     a.max_chunks = L.max_chunks;
+    a.f16 = op.io_dtype == KDA_IO_F16;
+    a.flags = op.beta_logits ? kIntraBetaLogits : 0;
+    a.group = dims->H / hqk;
     if (launch_intra(a, s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
-kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const kda_dims* dims,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const float* g,
+                         const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    return kda_fwd_intra_ex(q, k, v, g, beta, cu_seqlens, dims, nullptr, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd_scan_ex(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
+                           const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes,
+                           void* stream) {
     if (!dims) return KDA_ERR_INVALID_ARG;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    if (!check_opts(&op, dims)) return KDA_ERR_INVALID_ARG;
     const bool varlen = is_varlen(dims);
     kda_status st = check_dims(dims, varlen);
     if (st != KDA_OK) return st;
@@ -262,8 +288,14 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
     a.H = dims->H;
     a.K = dims->K;
     a.V = dims->V;
+    a.flags = (op.io_dtype == KDA_IO_F16 ? kScanOutF16 : 0) | (op.state_dtype == KDA_STATE_BF16 ? kScanStateBF16 : 0);
     if (launch_scan(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const kda_dims* dims,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    return kda_fwd_scan_ex(scale, h0, o, ht, dims, nullptr, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const float* dht, void* dhck, void* dv2,
@@ -308,12 +340,20 @@ kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const flo
     return KDA_OK;
 }
 
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                      float scale, const void* h0, const int32_t* cu_seqlens, void* o, void* ht,
+                      const kda_dims* dims, const kda_fwd_opts* opts, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    kda_status st = kda_fwd_intra_ex(q, k, v, g, beta, cu_seqlens, dims, opts, workspace, workspace_bytes, stream);
+    if (st != KDA_OK) return st;
+    return kda_fwd_scan_ex(scale, h0, o, ht, dims, opts, workspace, workspace_bytes, stream);
+}
+
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
                    float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
                    const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
-    kda_status st = kda_fwd_intra(q, k, v, g, beta, cu_seqlens, dims, workspace, workspace_bytes, stream);
-    if (st != KDA_OK) return st;
-    return kda_fwd_scan(scale, h0, o, ht, dims, workspace, workspace_bytes, stream);
+    return kda_fwd_ex(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, dims, nullptr, workspace, workspace_bytes,
+                      stream);
 }
 
 namespace {

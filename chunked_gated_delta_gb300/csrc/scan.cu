@@ -102,9 +102,9 @@ template <int KB, int NVB, int STAGES>
 __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB, NVB, STAGES>::MIN_CTAS)
     kda_scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_qg,
                     const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_u,
-                    const __grid_constant__ CUtensorMap tm_aqk, const float* __restrict__ h0,
-                    float* __restrict__ ht, uint16_t* __restrict__ o, uint8_t* __restrict__ ws,
-                    const WsLayout L, const float scale, const int H, const int V) {
+                    const __grid_constant__ CUtensorMap tm_aqk, const void* __restrict__ h0,
+                    void* __restrict__ ht, uint16_t* __restrict__ o, uint8_t* __restrict__ ws,
+                    const WsLayout L, const float scale, const int H, const int V, const int flags) {
     using S = ScanCfg<KB, NVB, STAGES>;
     constexpr int K = S::K;
     extern __shared__ uint8_t smem_raw[];
@@ -167,8 +167,21 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         const bool has_row = r < K;      // warp-uniform
         const int col = v0 + vb * 64;    // first V column of this warp's block
         float hreg[64];
-        if (has_row && h0 != nullptr) {
-            const float4* src = reinterpret_cast<const float4*>(h0 + (((int64_t)s * H + h) * K + r) * V + col);
+        const int64_t hrow = (((int64_t)s * H + h) * K + r) * V + col;  // element offset of this row
+        if (has_row && h0 != nullptr && (flags & kScanStateBF16)) {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(h0) + hrow);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 x = src[j];
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    hreg[8 * j + 2 * t] = bf_lo(xw[t]);
+                    hreg[8 * j + 2 * t + 1] = bf_hi(xw[t]);
+                }
+            }
+        } else if (has_row && h0 != nullptr) {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(h0) + hrow);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float4 x = src[j];
@@ -252,10 +265,18 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             write_h();
         }
         if (ht != nullptr && has_row && !timed_out && !*abort_flag) {
-            float4* dst = reinterpret_cast<float4*>(ht + (((int64_t)s * H + h) * K + r) * V + col);
+            if (flags & kScanStateBF16) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ht) + hrow);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_uint4(pack_bf16x2(hreg[8 * j], hreg[8 * j + 1]), pack_bf16x2(hreg[8 * j + 2], hreg[8 * j + 3]),
+                                        pack_bf16x2(hreg[8 * j + 4], hreg[8 * j + 5]), pack_bf16x2(hreg[8 * j + 6], hreg[8 * j + 7]));
+            } else {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(ht) + hrow);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
+            }
         }
     } else if (warp == S::TMA_WARP) {
         // ================= TMA producer =================
@@ -350,12 +371,21 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 if (i < valid) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         o + ((int64_t)(si.bos + c * 64 + i) * H + h) * V + v0 + vb * 64);
+                    if (flags & kScanOutF16) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_uint4(pack_bf16x2(scale * acc[8 * j], scale * acc[8 * j + 1]),
-                                            pack_bf16x2(scale * acc[8 * j + 2], scale * acc[8 * j + 3]),
-                                            pack_bf16x2(scale * acc[8 * j + 4], scale * acc[8 * j + 5]),
-                                            pack_bf16x2(scale * acc[8 * j + 6], scale * acc[8 * j + 7]));
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_uint4(pack_f16x2(scale * acc[8 * j], scale * acc[8 * j + 1]),
+                                                pack_f16x2(scale * acc[8 * j + 2], scale * acc[8 * j + 3]),
+                                                pack_f16x2(scale * acc[8 * j + 4], scale * acc[8 * j + 5]),
+                                                pack_f16x2(scale * acc[8 * j + 6], scale * acc[8 * j + 7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_uint4(pack_bf16x2(scale * acc[8 * j], scale * acc[8 * j + 1]),
+                                                pack_bf16x2(scale * acc[8 * j + 2], scale * acc[8 * j + 3]),
+                                                pack_bf16x2(scale * acc[8 * j + 4], scale * acc[8 * j + 5]),
+                                                pack_bf16x2(scale * acc[8 * j + 6], scale * acc[8 * j + 7]));
+                    }
                 }
             }
         }
@@ -380,7 +410,7 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t stream) {
     const int64_t ctas = (int64_t)a.N * a.H * (a.V / S::BV);
     if (ctas <= 0) return cudaSuccess;
     kern<<<(unsigned)ctas, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.h0,
-                                                       a.ht, a.o, a.ws, a.L, a.scale, a.H, a.V);
+                                                       a.ht, a.o, a.ws, a.L, a.scale, a.H, a.V, a.flags);
     return cudaGetLastError();
 }
 

@@ -122,3 +122,38 @@ def make_bwd_inputs(x: dict, seed: int = 0, dht: bool = True):
     dv_in = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
     dh_t = 0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32) if dht else None
     return dict(do=do, dv_in=dv_in, dht=dh_t)
+
+
+def make_variant_inputs(w: Workload, io_dtype=torch.bfloat16, qk_heads=None, beta_logits=False,
+                        state_dtype=torch.float32, lengths=None):
+    """Inputs of workload ``w`` for the forward's interface variants, drawn on
+    the CPU: q, k with ``qk_heads`` heads (default: w.H) and v, g, beta, h0 with
+    w.H heads; q, k, v, beta in ``io_dtype`` (bf16 or fp16); beta either in
+    (0, 1) (sigmoid of N(0,1)) or, with ``beta_logits``, the N(0,1) logits
+    themselves; h0 (when the workload has one) in ``state_dtype``.  Same
+    distributions as :func:`make_inputs` otherwise."""
+    gen = torch.Generator().manual_seed(w.seed + 104729)
+    if w.varlen or lengths is not None:
+        if lengths is None:
+            lengths = varlen_lengths(w.varlen, w.max_len, w.seed + 7919)
+        cu = cu_from_lengths(lengths)
+        B, T, N = 1, int(cu[-1]), len(lengths)
+    else:
+        cu = None
+        B, T, N = w.B, w.T, w.B
+    H, K, V = w.H, w.K, w.V
+    Hqk = H if qk_heads is None else qk_heads
+
+    def unit_rows(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(io_dtype)
+
+    q = unit_rows((B, T, Hqk, K))
+    k = unit_rows((B, T, Hqk, K))
+    v = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(io_dtype)
+    logits = torch.randn((B, T, H), generator=gen)
+    beta = (logits if beta_logits else torch.sigmoid(logits)).to(io_dtype)
+    g = F.logsigmoid(torch.randn((B, T, H, K), generator=gen) + w.mu)
+    h0 = (0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32)).to(state_dtype) if w.h0 else None
+    return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=K ** -0.5,
+                B=B, T=T, H=H, K=K, V=V, N=N, qk_heads=Hqk, beta_logits=beta_logits)

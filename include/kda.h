@@ -114,6 +114,52 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Interface variants of the forward.  A zero-initialised kda_fwd_opts (or a
+ * NULL pointer) gives exactly kda_fwd / kda_fwd_intra / kda_fwd_scan.
+ *   io_dtype     KDA_IO_BF16: q, k, v, beta and o are bf16.
+ *                KDA_IO_F16: they are fp16 (kernel-fun "kda/_kernels/fwd_state.py",
+ *                host wrapper: the io dtype is bf16 or fp16).  The
+ *                intermediates in the workspace stay bf16 either way.
+ *   state_dtype  KDA_STATE_F32: h0 and ht are fp32.  KDA_STATE_BF16: they are
+ *                bf16 (FlashKDA's StateFP32 = false, "KDA源码剖析之FlashKDA（下）",
+ *                initial / final state sections); the state is still carried
+ *                in fp32 on chip.
+ *   beta_logits  0: beta is given in (0, 1).  1: beta holds logits and the
+ *                kernel applies the sigmoid in fp32 (FlashKDA's in-kernel
+ *                sigmoid of beta).
+ *   qk_heads     heads of q and k; 0 means dims->H.  Otherwise dims->H (the
+ *                value heads: v, g, beta, o, h0, ht) must be a multiple of it,
+ *                and value head h reads q / k head h / (dims->H / qk_heads)
+ *                (grouped value heads, the "HV" heads of fwd_state.py).  q and
+ *                k are then [B, T, qk_heads, K].
+ * The ABI types: h0 / ht pointers are `const void*` / `void*` here because
+ * their element type follows state_dtype.  Invalid option values return
+ * KDA_ERR_INVALID_ARG.
+ */
+#define KDA_IO_BF16 0
+#define KDA_IO_F16 1
+#define KDA_STATE_F32 0
+#define KDA_STATE_BF16 1
+typedef struct kda_fwd_opts {
+    int32_t io_dtype;
+    int32_t state_dtype;
+    int32_t beta_logits;
+    int32_t qk_heads;
+} kda_fwd_opts;
+
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                      float scale, const void* h0, const int32_t* cu_seqlens, void* o, void* ht,
+                      const kda_dims* dims, const kda_fwd_opts* opts, void* workspace,
+                      size_t workspace_bytes, void* stream);
+kda_status kda_fwd_intra_ex(const void* q, const void* k, const void* v, const float* g,
+                            const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,
+                            const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes,
+                            void* stream);
+kda_status kda_fwd_scan_ex(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
+                           const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * Reverse state scan (the backward of the inter-chunk stage): the gradient of
  * the loss with respect to the recurrent state at every chunk boundary, after
  * kernel-fun "kda/_kernels/bwd_dhu.py".  With dh the gradient w.r.t. the state

@@ -140,3 +140,22 @@ def test_bwd_validation_errors_before_any_launch(lib):
     assert call_bwd(lib, d, do=FAKE + 2) == 3                           # misaligned do
     assert call_bwd(lib, d, dht=FAKE + 4) == 3                          # misaligned dht
     assert call_bwd(lib, d, dh0=FAKE + 8) == 3                          # misaligned dh0
+
+
+def test_fwd_ex_option_validation(lib):
+    P = ctypes.c_void_p
+    d = kda.make_dims(1, 128, 4, 128, 128)
+
+    def call(**kw):
+        o = kda.FwdOpts(**kw)
+        return lib.kda_fwd_ex(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0.1, None, None, P(FAKE), None,
+                              ctypes.byref(d), ctypes.byref(o), P(FAKE), 1 << 40, None)
+
+    assert call(io_dtype=2) == 1          # unknown io dtype
+    assert call(state_dtype=5) == 1       # unknown state dtype
+    assert call(beta_logits=2) == 1       # flag must be 0 / 1
+    assert call(qk_heads=3) == 1          # 4 value heads are not a multiple of 3
+    assert call(qk_heads=8) == 1          # more q/k heads than value heads
+    assert call(qk_heads=-1) == 1
+    assert lib.kda_fwd_scan_ex(0.1, None, P(FAKE), None, ctypes.byref(d), ctypes.byref(kda.FwdOpts(io_dtype=7)),
+                               P(FAKE), 1 << 40, None) == 1
