@@ -312,7 +312,8 @@ def run_gb300(args):
                           "frac_of_hbm_bound": (step_bytes / (hbm * 1e9) * 1e3) / ms_per_step},
         "kernels_ms": {"intra": intra_avg, "scan": scan_avg},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        # planner + intra + scan (+ map pass and combine when the scan is segmented)
+        "gpu_launches": (3 + (2 if kda.workspace_layout(dims).seg_count > 1 else 0)) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

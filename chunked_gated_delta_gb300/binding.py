@@ -53,7 +53,9 @@ STATE_F32, STATE_BF16 = 0, 1
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "seq_info", "chunk_info", "gd", "qg", "kg", "w", "u", "aqk", "total")] + [
-        ("max_chunks", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+        ("max_chunks", ctypes.c_int32), ("chunk", ctypes.c_int32),
+        ("seg_count", ctypes.c_int32), ("seg_len", ctypes.c_int32),
+        ("pq", ctypes.c_size_t), ("hin", ctypes.c_size_t)]
 
 
 def library_path() -> str:

@@ -41,9 +41,73 @@ inline int64_t max_chunks(const kda_dims& d, bool varlen) {
 }
 
 struct WsLayout {
-    size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, total;
+    size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, pq, hin, total;
     int64_t max_chunks;
+    int32_t seg_count;  // segments per sequence of the segmented scan (1 = plain scan)
+    int32_t seg_len;    // chunks per segment
 };
+
+// Scan kernel shape for a launch of ctas64 64-column blocks over ncol
+// columns per head (the same rule the launcher applies):
+//   few blocks          -> 64-column CTAs, two-stage ring, one per SM
+//   ncol % 128 == 0     -> 128-column CTAs, two-stage ring, one per SM
+//   otherwise           -> 64-column CTAs, one stage, two per SM
+// lat is the measured per-chunk latency of a CTA of that shape relative to
+// the first (1.4 / 2.2 / 2.3 us per chunk at K = 128 on GB300).
+struct ScanShape {
+    int nvb, stages, per_sm;
+    float lat;
+};
+inline ScanShape scan_shape(int64_t ctas64, int ncol, int sms) {
+    if (ctas64 <= sms) return {1, 2, 1, 1.0f};
+    if (ncol % 128 == 0) return {2, 2, 1, 1.6f};
+    return {1, 1, 2, 1.7f};
+}
+
+// Segmented scan plan.  When the plain scan would leave most SMs idle (few
+// sequences x heads over long sequences), each sequence's chunks are cut into
+// seg_count segments of seg_len chunks: a map pass computes every segment's
+// affine state map, a combine step chains them, and the output pass runs the
+// segments in parallel.  The plan models each choice as chunks per CTA x
+// relative per-chunk latency x waves (for an assumed kPlanSMs SMs), adds the
+// fixed cost of the extra launches, and segments only for a gain of at least
+// 10%; segments are never shorter than kSegMinChunks.  It depends on the dims
+// only (so does the workspace size).
+constexpr int kPlanSMs = 148;
+constexpr int kSegMinChunks = 16;
+constexpr int kSegMaxCount = 64;
+
+inline double scan_pass_cost(int64_t ctas64, int ncol) {
+    if (ctas64 <= 0) return 0.0;
+    const ScanShape sh = scan_shape(ctas64, ncol, kPlanSMs);
+    const int64_t ctas = ctas64 / sh.nvb;
+    const int64_t slots = (int64_t)kPlanSMs * sh.per_sm;
+    return (double)sh.lat * (double)((ctas + slots - 1) / slots);
+}
+
+inline void seg_plan(const kda_dims& d, bool varlen, int32_t* count, int32_t* len) {
+    const int64_t N = varlen ? d.num_seqs : d.B;
+    const int64_t units = N * d.H * (d.V / 64);
+    const int64_t maxt = (d.T + kChunk - 1) / kChunk;  // bound on any sequence's chunks
+    int64_t best_S = 1, best_L = maxt > 0 ? maxt : 1;
+    double best = (double)maxt * scan_pass_cost(units, d.V);
+    const double plain = best;
+    for (int64_t S = 2; S <= kSegMaxCount && units > 0 && S * kSegMinChunks <= maxt; ++S) {
+        const int64_t L = (maxt + S - 1) / S;
+        if ((maxt + L - 1) / L != S) continue;
+        const double cost = (double)L * (scan_pass_cost((S - 1) * N * d.H * ((d.K + d.V) / 64), d.K + d.V) +
+                                         scan_pass_cost(S * units, d.V)) +
+                            8.0 + 2.0 * (double)(S - 1);
+        if (cost < best) {
+            best = cost;
+            best_S = S;
+            best_L = L;
+        }
+    }
+    if (best_S > 1 && best > 0.9 * plain) best_S = 1;
+    *count = (int32_t)best_S;
+    *len = (int32_t)(best_S > 1 ? best_L : 0x7fffffff);
+}
 
 inline WsLayout ws_layout(const kda_dims& d, bool varlen) {
     WsLayout L{};
@@ -69,6 +133,12 @@ inline WsLayout ws_layout(const kda_dims& d, bool varlen) {
     off = align_up(off + tiles * kChunk * d.V * 2, 1024);
     L.aqk = off;
     off = align_up(off + tiles * kChunk * kChunk * 2, 1024);
+    seg_plan(d, varlen, &L.seg_count, &L.seg_len);
+    const size_t seg_units = L.seg_count > 1 ? (size_t)L.seg_count * N * d.H : 0;
+    L.pq = off;  // fp32 [S, N, H, K, K + V]: per segment [P | Q]
+    off = align_up(off + seg_units * d.K * (d.K + d.V) * sizeof(float), 1024);
+    L.hin = off;  // fp32 [S, N, H, K, V]: state entering each segment
+    off = align_up(off + seg_units * d.K * d.V * sizeof(float), 1024);
     L.total = off;
     L.max_chunks = NC;
     return L;

@@ -25,6 +25,8 @@ struct IntraArgs {
 constexpr int kIntraBetaLogits = 1;
 constexpr int kScanOutF16 = 1;     // o is fp16 (else bf16)
 constexpr int kScanStateBF16 = 2;  // h0 / ht are bf16 (else fp32)
+constexpr int kScanModeOutput = 0;  // the scan with its output o (and ht)
+constexpr int kScanModeMap = 1;     // per-segment affine maps [P | Q] (segmented scan)
 
 struct ScanArgs {
     CUtensorMap tm_w, tm_qg, tm_kg, tm_u, tm_aqk;  // workspace tiles, 2-D {dim, tiles*64}

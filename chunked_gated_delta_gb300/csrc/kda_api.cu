@@ -167,6 +167,10 @@ kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out) {
     out->total = L.total;
     out->max_chunks = (int32_t)L.max_chunks;
     out->chunk = kChunk;
+    out->seg_count = L.seg_count;
+    out->seg_len = L.seg_len;
+    out->pq = L.pq;
+    out->hin = L.hin;
     return KDA_OK;
 }
 

@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                     const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_aqk, const void* __restrict__ h0,
                     void* __restrict__ ht, uint16_t* __restrict__ o, uint8_t* __restrict__ ws,
-                    const WsLayout L, const float scale, const int H, const int V, const int flags) {
+                    const WsLayout L, const float scale, const int N, const int H, const int V, const int flags,
+                    const int mode) {
     using S = ScanCfg<KB, NVB, STAGES>;
     constexpr int K = S::K;
     extern __shared__ uint8_t smem_raw[];
@@ -112,15 +113,26 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                                              ~static_cast<uintptr_t>(1023));
     __shared__ ScanBars<STAGES> B;
 
-    const int NT = V / S::BV;  // V tiles per head
+    // Column space: V columns of h (output mode) or, in map mode, K + V
+    // columns [P | Q] of a segment's affine map h_out = P h_in + Q.
+    const bool map_mode = mode == kScanModeMap;
+    const int NCOL = map_mode ? K + V : V;
+    const int NT = NCOL / S::BV;  // column tiles per head
     const int vt = blockIdx.x % NT;
     const int h = (blockIdx.x / NT) % H;
     const int s = blockIdx.x / (NT * H);
+    const int seg = blockIdx.y;
     const int v0 = vt * S::BV;
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
     const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
     const int tiles = si.tiles;
+    // this CTA's chunks [c_begin, c_end) of the sequence
+    const int c_begin = seg * L.seg_len;
+    const int c_end = min(tiles, c_begin + L.seg_len);
+    if (seg > 0 && c_begin >= tiles) return;   // the sequence has fewer segments
+    if (map_mode && c_end >= tiles) return;    // the last segment's map is never used
+    const int nit = c_end > c_begin ? c_end - c_begin : 0;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
@@ -168,7 +180,23 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         const int col = v0 + vb * 64;    // first V column of this warp's block
         float hreg[64];
         const int64_t hrow = (((int64_t)s * H + h) * K + r) * V + col;  // element offset of this row
-        if (has_row && h0 != nullptr && (flags & kScanStateBF16)) {
+        // map mode: P columns start as the identity and see u = 0; Q columns start at 0
+        const bool p_block = map_mode && col < K;
+        if (map_mode) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) hreg[j] = (p_block && r == col + j) ? 1.f : 0.f;
+        } else if (seg > 0) {
+            const float4* src = reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(ws + L.hin) + ((((int64_t)seg * N + s) * H + h) * K + r) * V + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 x = has_row ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                hreg[4 * j] = x.x;
+                hreg[4 * j + 1] = x.y;
+                hreg[4 * j + 2] = x.z;
+                hreg[4 * j + 3] = x.w;
+            }
+        } else if (has_row && h0 != nullptr && (flags & kScanStateBF16)) {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(h0) + hrow);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -211,27 +239,28 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.h_ready);
         };
-        if (tiles > 0) write_h();
-        for (int c = 0; c < tiles && !*abort_flag; ++c) {
-            const int st = c % STAGES;
-            const uint32_t sp = (c / STAGES) & 1;
+        if (nit > 0) write_h();
+        for (int it = 0; it < nit && !*abort_flag; ++it) {
+            const int st = it % STAGES;
+            const uint32_t sp = (it / STAGES) & 1;
             uint8_t* stage = sm + st * S::STAGE;
             if (!wait(&B.full[st], sp)) break;
             if (quad < 2) {
                 // v'[r, :] = u[r, :] - WH[r, :]
-                if (!wait(&B.wh_full, c & 1)) break;
+                if (!wait(&B.wh_full, it & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16) {
                     float wh[16];
-                    tmem_ld16(t_acc + (uint32_t)((c & 1) * S::BV + vb * 64) + ((uint32_t)(quad * 32) << 16) + c0,
+                    tmem_ld16(t_acc + (uint32_t)((it & 1) * S::BV + vb * 64) + ((uint32_t)(quad * 32) << 16) + c0,
                               wh);
                     tmem_ld_wait();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = (c0 >> 3) + hh;
                         const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
-                        const uint4 uv = *reinterpret_cast<const uint4*>(stage + S::U + vb * 8192 + off);
+                        const uint4 uv = p_block ? make_uint4(0u, 0u, 0u, 0u)
+                                                 : *reinterpret_cast<const uint4*>(stage + S::U + vb * 8192 + off);
                         const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
                         uint32_t pw[4];
 #pragma unroll
@@ -247,7 +276,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 if (lane == 0) mbar_arrive(&B.vp_ready);
             }
             const float decay = has_row ? ex2(reinterpret_cast<const float*>(stage + S::GD)[r]) : 0.f;
-            if (!wait(&B.dh_full, c & 1)) break;
+            if (!wait(&B.dh_full, it & 1)) break;
             tc_fence_after();
             if (has_row) {
 #pragma unroll
@@ -264,7 +293,13 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             if (lane == 0) mbar_arrive(&B.empty[st]);
             write_h();
         }
-        if (ht != nullptr && has_row && !timed_out && !*abort_flag) {
+        if (map_mode && has_row && !timed_out && !*abort_flag) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(ws + L.pq) +
+                                                    ((((int64_t)seg * N + s) * H + h) * K + r) * (K + V) + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
+        } else if (!map_mode && c_end == tiles && ht != nullptr && has_row && !timed_out && !*abort_flag) {
             if (flags & kScanStateBF16) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ht) + hrow);
 #pragma unroll
@@ -280,31 +315,44 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         }
     } else if (warp == S::TMA_WARP) {
         // ================= TMA producer =================
-        if (lane == 0 && tiles > 0) {
+        if (lane == 0 && nit > 0) {
             prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_qg);
             prefetch_tmap(&tm_kg);
             prefetch_tmap(&tm_u);
             prefetch_tmap(&tm_aqk);
             const float* gd = reinterpret_cast<const float*>(ws + L.gd);
-            for (int c = 0; c < tiles && !*abort_flag; ++c) {
-                const int st = c % STAGES;
-                const uint32_t sp = (c / STAGES) & 1;
+            // map mode reads neither qg nor Aqk (no output) nor u for P columns
+            uint32_t tx = S::TX_BYTES;
+            if (map_mode) {
+                tx -= (KB + 1) * 8192;
+#pragma unroll
+                for (int vb = 0; vb < NVB; ++vb)
+                    if (v0 + vb * 64 < K) tx -= 8192;
+            }
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
+                const int c = c_begin + it;
+                const int st = it % STAGES;
+                const uint32_t sp = (it / STAGES) & 1;
                 if (!wait(&B.empty[st], sp ^ 1)) break;
                 uint8_t* stage = sm + st * S::STAGE;
                 const int64_t tile = (int64_t)(si.tile_base + c) * H + h;
                 const int row = (int)(tile * 64);
                 uint64_t* fb = &B.full[st];
-                mbar_arrive_expect_tx(fb, S::TX_BYTES);
+                mbar_arrive_expect_tx(fb, tx);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_2d(stage + S::AW + kb * 16384, &tm_w, fb, kb * 64, row);
-                    tma_load_2d(stage + S::AW + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
+                    if (!map_mode) tma_load_2d(stage + S::AW + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
                     tma_load_2d(stage + S::KG + kb * 8192, &tm_kg, fb, kb * 64, row);
                 }
-                tma_load_2d(stage + S::AQK, &tm_aqk, fb, 0, row);
+                if (!map_mode) tma_load_2d(stage + S::AQK, &tm_aqk, fb, 0, row);
 #pragma unroll
-                for (int vb = 0; vb < NVB; ++vb) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, v0 + vb * 64, row);
+                for (int vb = 0; vb < NVB; ++vb) {
+                    const int cb = v0 + vb * 64;
+                    if (!map_mode) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, cb, row);
+                    else if (cb >= K) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, cb - K, row);
+                }
                 bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
             }
         }
@@ -313,14 +361,14 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         if (lane == 0) {
             constexpr uint32_t id_h = idesc_bf16_f32(128, S::BV, 0, 1);   // A K-major, B (h, v') MN-major
             constexpr uint32_t id_dh = idesc_bf16_f32(128, S::BV, 1, 1);  // A = kg^T MN-major
-            for (int c = 0; c < tiles && !*abort_flag; ++c) {
-                const int st = c % STAGES;
-                const uint32_t sp = (c / STAGES) & 1;
-                const int buf = c & 1;
-                const uint32_t bp = (c >> 1) & 1;
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
+                const int st = it % STAGES;
+                const uint32_t sp = (it / STAGES) & 1;
+                const int buf = it & 1;
+                const uint32_t bp = (it >> 1) & 1;
                 const uint32_t stage = sbase + st * S::STAGE;
                 if (!wait(&B.full[st], sp)) break;
-                if (!wait(&B.h_ready, c & 1)) break;
+                if (!wait(&B.h_ready, it & 1)) break;
                 if (!wait(&B.acc_empty[buf], bp ^ 1)) break;
                 tc_fence_after();
                 const uint32_t d_acc = t_acc + buf * S::BV;
@@ -331,17 +379,19 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                              smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_h, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&B.wh_full);
-                if (!wait(&B.vp_ready, c & 1)) break;
+                if (!wait(&B.vp_ready, it & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(t_dh, smem_desc(stage + S::KG + ks * 2048, 8192, 1024),
                              smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_dh, ks > 0 ? 1u : 0u);
                 mma_commit(&B.dh_full);
+                if (!map_mode) {
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(d_acc, smem_desc(stage + S::AQK - 8192 + ks * 32, 16, 1024),
-                             smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_h, 1u);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(d_acc, smem_desc(stage + S::AQK - 8192 + ks * 32, 16, 1024),
+                                 smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_h, 1u);
+                }
                 mma_commit(&B.acc_full[buf]);
                 mma_commit(&B.empty[st]);
             }
@@ -353,11 +403,18 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             const int quad = 2 + (e & 1);          // TMEM lanes 64..127
             const int vb = e >> 1;
             const int i = (quad - 2) * 32 + lane;  // token row within the chunk
-            for (int c = 0; c < tiles && !*abort_flag; ++c) {
-                const int buf = c & 1;
-                const uint32_t bp = (c >> 1) & 1;
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
+                const int c = c_begin + it;
+                const int buf = it & 1;
+                const uint32_t bp = (it >> 1) & 1;
                 if (!wait(&B.acc_full[buf], bp)) break;
                 tc_fence_after();
+                if (map_mode) {  // no output: hand the accumulator back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&B.acc_empty[buf]);
+                    continue;
+                }
                 float acc[64];
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16)
@@ -401,29 +458,155 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
 }
 
 template <int KB, int NVB, int STAGES>
-cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t stream) {
+cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream) {
     using S = ScanCfg<KB, NVB, STAGES>;
     const uint32_t smem = S::BYTES + 1024;
     auto kern = kda_scan_kernel<KB, NVB, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int64_t ctas = (int64_t)a.N * a.H * (a.V / S::BV);
-    if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.h0,
-                                                       a.ht, a.o, a.ws, a.L, a.scale, a.H, a.V, a.flags);
+    const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
+    const int64_t ctas = (int64_t)a.N * a.H * (ncol / S::BV);
+    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    if (ctas <= 0 || segs <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)ctas, (unsigned)segs);
+    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.h0, a.ht, a.o, a.ws,
+                                             a.L, a.scale, a.N, a.H, a.V, a.flags, mode);
     return cudaGetLastError();
 }
 
 template <int KB>
-cudaError_t launch_scan_k(const ScanArgs& a, cudaStream_t stream, int sms) {
-    const int64_t ctas64 = (int64_t)a.N * a.H * (a.V / 64);
+cudaError_t launch_scan_k(const ScanArgs& a, int mode, cudaStream_t stream, int sms) {
+    const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
+    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const ScanShape sh = scan_shape((int64_t)a.N * a.H * (ncol / 64) * segs, ncol, sms);
     // Few CTAs: each SM holds at most one, so give it a two-deep input ring.
-    if (ctas64 <= sms) return launch_scan_t<KB, 1, 2>(a, stream);
-    // Many CTAs with V = 128: one CTA per (sequence, head) covering all of V,
-    // two-deep ring, w/qg/kg/Aqk loaded once per head.
-    if (a.V % 128 == 0) return launch_scan_t<KB, 2, 2>(a, stream);
-    // Many CTAs with V = 64: two CTAs per SM, one stage each.
-    return launch_scan_t<KB, 1, 1>(a, stream);
+    if (sh.nvb == 1 && sh.stages == 2) return launch_scan_t<KB, 1, 2>(a, mode, stream);
+    // Many CTAs with 128-column tiles: one CTA covers 128 columns, two-deep
+    // ring, w/qg/kg/Aqk loaded once per 128 columns.
+    if (sh.nvb == 2) return launch_scan_t<KB, 2, 2>(a, mode, stream);
+    // Many CTAs otherwise: two CTAs per SM, one stage each.
+    return launch_scan_t<KB, 1, 1>(a, mode, stream);
+}
+
+// Chains the segment maps of the map pass: for every (sequence, head, 16
+// columns of V), h_in[0] = h0 and h_in[j+1] = P_j h_in[j] + Q_j in fp32, for
+// the segments the sequence has.  Thread r owns state row r and its 16
+// columns.  P_j (K x K) streams into a double buffer by cp.async while the
+// previous step computes; its rows keep their 16-byte chunks XOR-swizzled by
+// (row & 7), so the float4 row reads of 8 consecutive threads hit distinct
+// banks.  h_in[j] (K x 16) is double-buffered and read as broadcast float4s.
+constexpr int kCombineCols = 16;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int K>
+__global__ void __launch_bounds__(128) kda_seg_combine_kernel(const void* __restrict__ h0, uint8_t* __restrict__ ws,
+                                                              const WsLayout L, const int N, const int H, const int V,
+                                                              const int flags) {
+    constexpr int C = kCombineCols, K4 = K / 4;
+    extern __shared__ float4 csm4[];
+    float4* Ps = csm4;              // 2 x [K][K / 4], chunk-swizzled rows
+    float4* Hs = csm4 + 2 * K * K4;  // 2 x [K][C / 4]
+    const int NTV = V / C;
+    const int vt = blockIdx.x % NTV, h = (blockIdx.x / NTV) % H, s = blockIdx.x / (NTV * H);
+    const int32_t* status = reinterpret_cast<const int32_t*>(ws + L.status);
+    if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
+    const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
+    const int nseg = (si.tiles + L.seg_len - 1) / L.seg_len;
+    if (nseg < 2) return;
+    const int tid = threadIdx.x;
+    const int col0 = vt * C;
+    const int r = tid;  // state row
+    const float* pq = reinterpret_cast<const float*>(ws + L.pq);
+    float* hin = reinterpret_cast<float*>(ws + L.hin);
+    auto map_of = [&](int j) { return pq + (((int64_t)j * N + s) * H + h) * K * (K + V); };
+    auto stage_p = [&](int j) {  // issue the copies of P_j into buffer j & 1
+        const float* PQ = map_of(j);
+        float4* dst = Ps + (j & 1) * K * K4;
+        for (int e4 = tid; e4 < K * K4; e4 += 128) {
+            const int row = e4 / K4, c4 = e4 % K4;
+            cp_async16(dst + row * K4 + (c4 ^ (row & 7)), PQ + (int64_t)row * (K + V) + 4 * c4);
+        }
+        cp_async_commit();
+    };
+    stage_p(0);
+    if (r < K) {
+        float hr[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            float x = 0.f;
+            if (h0 != nullptr) {
+                const int64_t off = (((int64_t)s * H + h) * K + r) * V + col0 + c;
+                x = (flags & kScanStateBF16)
+                        ? __uint_as_float(((uint32_t) static_cast<const uint16_t*>(h0)[off]) << 16)
+                        : static_cast<const float*>(h0)[off];
+            }
+            hr[c] = x;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < C / 4; ++c4)
+            Hs[r * (C / 4) + c4] = make_float4(hr[4 * c4], hr[4 * c4 + 1], hr[4 * c4 + 2], hr[4 * c4 + 3]);
+    }
+    for (int j = 0; j + 1 < nseg; ++j) {
+        if (j + 2 < nseg) {
+            stage_p(j + 1);  // overlaps this step
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const float4* P = Ps + (j & 1) * K * K4;
+        const float4* Hc = Hs + (j & 1) * K * (C / 4);
+        float4* Hn = Hs + ((j + 1) & 1) * K * (C / 4);
+        if (r < K) {
+            const float* PQ = map_of(j);
+            float acc[C];
+            const float* q = PQ + (int64_t)r * (K + V) + K + col0;
+#pragma unroll
+            for (int c = 0; c < C; ++c) acc[c] = q[c];
+#pragma unroll 2
+            for (int k4 = 0; k4 < K4; ++k4) {
+                const float4 p4 = P[r * K4 + (k4 ^ (r & 7))];
+                const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                    for (int c4 = 0; c4 < C / 4; ++c4) {
+                        const float4 x = Hc[(4 * k4 + kk) * (C / 4) + c4];
+                        acc[4 * c4] = fmaf(pk[kk], x.x, acc[4 * c4]);
+                        acc[4 * c4 + 1] = fmaf(pk[kk], x.y, acc[4 * c4 + 1]);
+                        acc[4 * c4 + 2] = fmaf(pk[kk], x.z, acc[4 * c4 + 2]);
+                        acc[4 * c4 + 3] = fmaf(pk[kk], x.w, acc[4 * c4 + 3]);
+                    }
+                }
+            }
+            float4* dst = reinterpret_cast<float4*>(hin + ((((int64_t)(j + 1) * N + s) * H + h) * K + r) * V + col0);
+#pragma unroll
+            for (int c4 = 0; c4 < C / 4; ++c4) {
+                const float4 x = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
+                Hn[r * (C / 4) + c4] = x;
+                dst[c4] = x;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int K>
+cudaError_t launch_combine_k(const ScanArgs& a, cudaStream_t stream) {
+    const uint32_t smem = (2 * K * (K / 4) + 2 * K * (kCombineCols / 4)) * sizeof(float4);
+    auto kern = kda_seg_combine_kernel<K>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = (int64_t)a.N * a.H * (a.V / kCombineCols);
+    if (ctas <= 0) return cudaSuccess;
+    kern<<<(unsigned)ctas, 128, smem, stream>>>(a.h0, a.ws, a.L, a.N, a.H, a.V, a.flags);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -433,9 +616,19 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         sms = 148;
-    if (a.K == 128) return launch_scan_k<2>(a, stream, sms);
-    if (a.K == 64) return launch_scan_k<1>(a, stream, sms);
-    return cudaErrorInvalidValue;
+    if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
+    auto run = [&](int mode) {
+        return a.K == 128 ? launch_scan_k<2>(a, mode, stream, sms) : launch_scan_k<1>(a, mode, stream, sms);
+    };
+    if (a.L.seg_count > 1) {
+        // segmented: maps of every segment but the last, chain them, then the
+        // output pass over all segments in parallel
+        cudaError_t e = run(kScanModeMap);
+        if (e != cudaSuccess) return e;
+        e = a.K == 128 ? launch_combine_k<128>(a, stream) : launch_combine_k<64>(a, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return run(kScanModeOutput);
 }
 
 }  // namespace kda

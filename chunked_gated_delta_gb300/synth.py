@@ -58,6 +58,9 @@ WORKLOADS = {
     # the same token-heads as "quarter" spread over 128 heads: the scan kernel
     # runs the headline's grid (128 CTAs, 128-wide V tiles) on 32 chunks each
     "wide": Workload("wide", B=1, T=2048, H=128, K=128, V=128, seed=20261208),
+    # the long single sequence at head dim 64
+    "long_k64": Workload("long_k64", B=1, T=65536, H=32, K=64, V=64, mu=5.0, h0=False,
+                         seed=20261209),
 }
 
 

@@ -284,6 +284,14 @@ typedef struct kda_ws_layout {
     size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, total;
     int32_t max_chunks;
     int32_t chunk;
+    /* Segmented scan (few sequences x heads over long sequences): each
+     * sequence's chunks are cut into seg_count segments of seg_len chunks;
+     * pq holds every segment's affine state map [P | Q] (fp32 [seg_count, N,
+     * H, K, K + V]) and hin the state entering each segment (fp32 [seg_count,
+     * N, H, K, V]).  seg_count = 1: the plain scan (pq, hin empty). */
+    int32_t seg_count;
+    int32_t seg_len;
+    size_t pq, hin;
 } kda_ws_layout;
 kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out);
 

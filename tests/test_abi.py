@@ -159,3 +159,27 @@ def test_fwd_ex_option_validation(lib):
     assert call(qk_heads=-1) == 1
     assert lib.kda_fwd_scan_ex(0.1, None, P(FAKE), None, ctypes.byref(d), ctypes.byref(kda.FwdOpts(io_dtype=7)),
                                P(FAKE), 1 << 40, None) == 1
+
+
+def test_segmented_scan_plan():
+    """The scan is cut into segments only when few (sequence, head, 64-column)
+    units would leave most SMs idle over long sequences and the plan's cost
+    model expects a gain; the plan depends on the dims alone."""
+    lay = kda.workspace_layout(kda.make_dims(4, 8192, 32, 128, 128))     # headline: 256 units
+    assert lay.seg_count == 1 and lay.pq == lay.hin == lay.total
+    lay = kda.workspace_layout(kda.make_dims(1, 65536, 32, 128, 128))    # long: one wave already
+    assert lay.seg_count == 1
+    lay = kda.workspace_layout(kda.make_dims(1, 65536, 32, 64, 64))      # long, K = V = 64: 32 units
+    assert lay.seg_count == 9 and lay.seg_len == 114
+    assert lay.hin - lay.pq == 9 * 32 * 64 * 128 * 4
+    assert lay.total - lay.hin == 9 * 32 * 64 * 64 * 4
+    lay = kda.workspace_layout(kda.make_dims(1, 4096, 16, 128, 128))     # mid
+    assert lay.seg_count == 4 and lay.seg_len == 16
+    lay = kda.workspace_layout(kda.make_dims(1, 1000, 2, 128, 128))      # too short to cut
+    assert lay.seg_count == 1
+    lay = kda.workspace_layout(kda.make_dims(1, 10049, 2, 128, 128, num_seqs=5))   # varlen bound
+    assert lay.seg_count == 7 and lay.seg_len == 23
+    for d in (kda.make_dims(1, 65536, 32, 64, 64), kda.make_dims(2, 6405, 1, 64, 64)):
+        lay = kda.workspace_layout(d)
+        chunks = (d.T + 63) // 64  # every segment holds at least one chunk, together all of them
+        assert (lay.seg_count - 1) * lay.seg_len < chunks <= lay.seg_count * lay.seg_len
