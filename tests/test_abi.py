@@ -169,17 +169,18 @@ def test_segmented_scan_plan():
     assert lay.seg_count == 1 and lay.pq == lay.hin == lay.total
     lay = kda.workspace_layout(kda.make_dims(1, 65536, 32, 128, 128))    # long: one wave already
     assert lay.seg_count == 1
-    lay = kda.workspace_layout(kda.make_dims(1, 65536, 32, 64, 64))      # long, K = V = 64: 32 units
-    assert lay.seg_count == 9 and lay.seg_len == 114
-    assert lay.hin - lay.pq == 9 * 32 * 64 * 128 * 4
-    assert lay.total - lay.hin == 9 * 32 * 64 * 64 * 4
-    lay = kda.workspace_layout(kda.make_dims(1, 4096, 16, 128, 128))     # mid
-    assert lay.seg_count == 4 and lay.seg_len == 16
     lay = kda.workspace_layout(kda.make_dims(1, 1000, 2, 128, 128))      # too short to cut
     assert lay.seg_count == 1
-    lay = kda.workspace_layout(kda.make_dims(1, 10049, 2, 128, 128, num_seqs=5))   # varlen bound
-    assert lay.seg_count == 7 and lay.seg_len == 23
-    for d in (kda.make_dims(1, 65536, 32, 64, 64), kda.make_dims(2, 6405, 1, 64, 64)):
+    cases = [kda.make_dims(1, 65536, 32, 64, 64),                        # long at K = V = 64: 32 units
+             kda.make_dims(1, 4096, 16, 128, 128),                       # mid
+             kda.make_dims(2, 6405, 1, 64, 64),
+             kda.make_dims(1, 10049, 2, 128, 128, num_seqs=5)]           # varlen bound
+    for d in cases:
         lay = kda.workspace_layout(d)
+        n = d.num_seqs if d.num_seqs > 0 else d.B
+        S = lay.seg_count
+        assert S >= 2 and lay.seg_len >= 16
         chunks = (d.T + 63) // 64  # every segment holds at least one chunk, together all of them
-        assert (lay.seg_count - 1) * lay.seg_len < chunks <= lay.seg_count * lay.seg_len
+        assert (S - 1) * lay.seg_len < chunks <= S * lay.seg_len
+        assert lay.hin - lay.pq == S * n * d.H * d.K * (d.K + d.V) * 4
+        assert lay.total - lay.hin == S * n * d.H * d.K * d.V * 4
