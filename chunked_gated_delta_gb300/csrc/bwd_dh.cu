@@ -227,13 +227,13 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             tc_fence_after();
             if (has_row) {
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    float qd[16], wd[16];
-                    tmem_ld16(t_qd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, qd);
-                    tmem_ld16(t_wd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, wd);
+                for (int c0 = 0; c0 < 64; c0 += 8) {
+                    float qd[8], wd[8];
+                    tmem_ld8(t_qd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, qd);
+                    tmem_ld8(t_wd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, wd);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) dh[c0 + t] = fmaf(decay, dh[c0 + t], fmaf(scale, qd[t], -wd[t]));
+                    for (int t = 0; t < 8; ++t) dh[c0 + t] = fmaf(decay, dh[c0 + t], fmaf(scale, qd[t], -wd[t]));
                 }
             }
             tc_fence_before();

@@ -68,9 +68,6 @@ __device__ __forceinline__ float ex2(float x) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float bf16_at(const uint8_t* p) {
-    return __uint_as_float(((uint32_t)(*(const uint16_t*)p)) << 16);
-}
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 // Inputs q, k, v, beta are bf16 or (F16) fp16; everything computed on chip and
@@ -175,22 +172,27 @@ struct IntraSmem {
     static constexpr uint32_t KI = GV;
     static constexpr uint32_t VS = GV + 16384;
     static constexpr uint32_t GV_BYTES = (64 * K * 4 > 16384 + VB * 8192) ? 64 * K * 4 : 16384 + VB * 8192;
-    static constexpr uint32_t PART = GV + GV_BYTES;      // segment sums fp32 [NSEG][K]
-    static constexpr uint32_t XS = PART + NSEG * K * 4;  // per-warp X halves fp32 [6][16][8]
+    // segment sums fp32 [NSEG][K] (cumsum passes only): own 4 KB when K = 128;
+    // when K = 64 they use the extra T region, which is free until the inverse
+    static constexpr uint32_t PART_OWN = GV + GV_BYTES;
+    static constexpr uint32_t XS = KB == 2 ? PART_OWN + NSEG * K * 4 : PART_OWN;  // X halves fp32 [6][16][8]
     static constexpr uint32_t BETA = XS + 6 * 512;       // beta fp32 [64]
     // rows 32..63 of T: the second qg slot when K = 128, an extra 8 KB when K = 64
     static constexpr uint32_t TMHI = KB == 2 ? QK + 16384 : BETA + 256;
+    static constexpr uint32_t PART = KB == 2 ? PART_OWN : TMHI;
     static constexpr uint32_t END = KB == 2 ? BETA + 256 : TMHI + 8192;
     // the transposed w/u MMAs with K or V = 64 read 8 KB past their operand (unused rows)
     static constexpr uint32_t BYTES = END > VS + 16384 ? END : VS + 16384;
     static constexpr uint32_t QK_TX = 2 * KB * 8192, G_TX = 64 * K * 4, V_TX = VB * 8192;
     static_assert(NSEG * K * 4 == 4096, "segment sums are 4 KB");
+    static_assert(KB == 2 || NSEG * K * 4 <= 8192, "segment sums fit the extra T region");
 };
 
 // flags: kIntraBetaLogits = beta holds logits (sigmoid applied here).
 // group: value heads per q/k head (value head h reads q/k head h / group).
+// Three CTAs per SM; four at K = V = 64 (55 KB of shared memory, 64 registers).
 template <int KB, int VB, bool F16>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap st_qg, const __grid_constant__ CUtensorMap st_w,
