@@ -28,6 +28,14 @@
 // The chain DV -> dv2 -> WD -> dh -> next DV is issued first; QD overlaps it.
 // Rows of a tail chunk past the sequence end have qg = kg = w = 0 in the
 // workspace, so do there contributes nothing; dv2 rows there are masked.
+//
+// Segmented (few sequences x heads over long sequences, the forward's plan):
+// the reverse update is affine in dh, dh_in = (Diag(2^G) - w^T kg) dh_out +
+// (scale qg^T do - w^T dv_in), so a map pass runs every segment but the
+// oldest from [I | 0] over K + V columns (do = dv_in = 0 on the P columns)
+// and stores [P | Q]; the forward's combine kernel chains them newest first
+// from dht; the output pass runs all segments in parallel from their entry
+// gradients, each writing its own checkpoints and dv2 rows, the oldest dh0.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -93,7 +101,8 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_dvin, const float* __restrict__ dht,
                       uint16_t* __restrict__ dhck, uint16_t* __restrict__ dv2, float* __restrict__ dh0,
-                      uint8_t* __restrict__ ws, const WsLayout L, const float scale, const int H, const int V) {
+                      uint8_t* __restrict__ ws, const WsLayout L, const float scale, const int N, const int H,
+                      const int V, const int mode) {
     using S = BwdCfg<KB, NVB, STAGES>;
     constexpr int K = S::K;
     extern __shared__ uint8_t smem_raw[];
@@ -101,7 +110,11 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                                              ~static_cast<uintptr_t>(1023));
     __shared__ BwdBars<STAGES> B;
 
-    const int NT = V / S::BV;
+    // Column space: V columns of dh (output mode) or, in map mode, K + V
+    // columns [P | Q] of a segment's affine map dh_in = P dh_out + Q.
+    const bool map_mode = mode == kScanModeMap;
+    const int NCOL = map_mode ? K + V : V;
+    const int NT = NCOL / S::BV;
     const int vt = blockIdx.x % NT;
     const int h = (blockIdx.x / NT) % H;
     const int s = blockIdx.x / (NT * H);
@@ -110,6 +123,16 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
     if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
     const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
     const int tiles = si.tiles;
+    // segments of the sequence (all of it when the scan is not segmented);
+    // the map pass covers segments 1.., the output pass segments 0..
+    const int nseg = tiles == 0 ? 0 : (tiles - 1) / L.seg_len + 1;
+    const int seg = map_mode ? (int)blockIdx.y + 1 : (int)blockIdx.y;
+    if (seg > 0 && seg >= nseg) return;
+    const int c_lo = seg * L.seg_len;                 // this CTA's chunks [c_lo, c_hi),
+    const int c_hi = min(tiles, c_lo + L.seg_len);    // walked newest first
+    const int nit = c_hi > c_lo ? c_hi - c_lo : 0;
+    // the segment maps and entry states are stored newest segment first
+    const int rev = nseg - 1 - seg;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
@@ -129,6 +152,19 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
     if (warp == S::MMA_WARP) {
         tmem_alloc(&B.tmem_slot, S::TMEM_COLS);
         tmem_relinquish();
+    }
+    if (map_mode) {
+        // P columns see do = dv_in = 0: their tiles stay zero in every stage
+        // (the TMA never writes them)
+        for (int st = 0; st < STAGES; ++st)
+#pragma unroll
+            for (int b = 0; b < NVB; ++b)
+                if (v0 + b * 64 < K)
+                    for (int e = tid; e < 1024; e += S::THREADS) {
+                        reinterpret_cast<uint4*>(sm + st * S::STAGE + S::DO + b * 8192)[e] = make_uint4(0u, 0u, 0u, 0u);
+                        reinterpret_cast<uint4*>(sm + st * S::STAGE + S::DVIN + b * 8192)[e] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -151,8 +187,18 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         const bool has_row = r < K;      // warp-uniform
         const int col = v0 + vb * 64;
         float dh[64];
-        if (has_row && dht != nullptr) {
-            const float4* src = reinterpret_cast<const float4*>(dht + (((int64_t)s * H + h) * K + r) * V + col);
+        // start: map mode [I | 0]; the newest segment dht (or 0); any other
+        // segment the entry state the combine step chained for it
+        const float* src_row = nullptr;
+        if (!map_mode && has_row) {
+            if (seg == nseg - 1 || nseg == 0) {
+                if (dht != nullptr) src_row = dht + (((int64_t)s * H + h) * K + r) * V + col;
+            } else {
+                src_row = reinterpret_cast<const float*>(ws + L.hin) + ((((int64_t)rev * N + s) * H + h) * K + r) * V + col;
+            }
+        }
+        if (src_row != nullptr) {
+            const float4* src = reinterpret_cast<const float4*>(src_row);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float4 x = src[j];
@@ -163,18 +209,18 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) dh[j] = 0.f;
+            for (int j = 0; j < 64; ++j) dh[j] = (map_mode && has_row && r == col + j) ? 1.f : 0.f;
         }
         uint8_t* hs = sm + S::HS + vb * S::HS_BLOCK;
         uint8_t* vp = sm + S::VP + vb * 8192;
-        for (int it = 0; it < tiles && !*abort_flag; ++it) {
-            const int c = tiles - 1 - it;
+        for (int it = 0; it < nit && !*abort_flag; ++it) {
+            const int c = c_hi - 1 - it;
             const int st = it % STAGES;
             const uint32_t sp = (it / STAGES) & 1;
             uint8_t* stage = sm + st * S::STAGE;
             // checkpoint and MMA operand: dh before this chunk's update, bf16
             if (has_row) {
-                uint4* ck = dhck == nullptr ? nullptr
+                uint4* ck = (dhck == nullptr || map_mode) ? nullptr
                                             : reinterpret_cast<uint4*>(
                                                   dhck + (((int64_t)(si.tile_base + c) * H + h) * K + r) * V + col);
 #pragma unroll
@@ -214,7 +260,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                                            : 0u;
                         const uint4 x = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                         *reinterpret_cast<uint4*>(vp + off) = x;
-                        if (row_ok) gdst[cc] = x;
+                        if (row_ok && !map_mode) gdst[cc] = x;
                     }
                 }
                 fence_proxy_async_smem();
@@ -240,22 +286,31 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.empty[st]);
         }
-        if (dh0 != nullptr && has_row && !timed_out && !*abort_flag) {
+        if (map_mode && has_row && !timed_out && !*abort_flag) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(ws + L.pq) +
+                                                    ((((int64_t)rev * N + s) * H + h) * K + r) * (K + V) + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
+        } else if (!map_mode && seg == 0 && dh0 != nullptr && has_row && !timed_out && !*abort_flag) {
             float4* dst = reinterpret_cast<float4*>(dh0 + (((int64_t)s * H + h) * K + r) * V + col);
 #pragma unroll
             for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
         }
     } else if (warp == S::TMA_WARP) {
         // ================= TMA producer =================
-        if (lane == 0 && tiles > 0) {
+        if (lane == 0 && nit > 0) {
             prefetch_tmap(&tm_kg);
             prefetch_tmap(&tm_qg);
             prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_do);
             prefetch_tmap(&tm_dvin);
             const float* gd = reinterpret_cast<const float*>(ws + L.gd);
-            for (int it = 0; it < tiles && !*abort_flag; ++it) {
-                const int c = tiles - 1 - it;
+            uint32_t tx = S::TX_BYTES;  // map mode: no do / dv_in for P columns
+#pragma unroll
+            for (int b = 0; b < NVB; ++b)
+                if (map_mode && v0 + b * 64 < K) tx -= 2 * 8192;
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
+                const int c = c_hi - 1 - it;
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
                 if (!wait(&B.empty[st], sp ^ 1)) break;
@@ -264,7 +319,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 const int row = (int)(tile * 64);
                 const int trow = si.bos + c * 64;
                 uint64_t* fb = &B.full[st];
-                mbar_arrive_expect_tx(fb, S::TX_BYTES);
+                mbar_arrive_expect_tx(fb, tx);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_2d(stage + S::AKQ + kb * 16384, &tm_kg, fb, kb * 64, row);
@@ -273,8 +328,10 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 }
 #pragma unroll
                 for (int vb = 0; vb < NVB; ++vb) {
-                    tma_load_3d(stage + S::DO + vb * 8192, &tm_do, fb, v0 + vb * 64, h, trow);
-                    tma_load_3d(stage + S::DVIN + vb * 8192, &tm_dvin, fb, v0 + vb * 64, h, trow);
+                    const int cb = v0 + vb * 64, uc = map_mode ? cb - K : cb;  // column in the user tensors
+                    if (uc < 0) continue;
+                    tma_load_3d(stage + S::DO + vb * 8192, &tm_do, fb, uc, h, trow);
+                    tma_load_3d(stage + S::DVIN + vb * 8192, &tm_dvin, fb, uc, h, trow);
                 }
                 bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
             }
@@ -284,7 +341,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         if (lane == 0) {
             constexpr uint32_t id_dv = idesc_bf16_f32(128, S::BV, 0, 1);  // A K-major, B (dh) MN-major
             constexpr uint32_t id_up = idesc_bf16_f32(128, S::BV, 1, 1);  // A (qg^T, w^T) MN-major
-            for (int it = 0; it < tiles && !*abort_flag; ++it) {
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
                 const uint32_t stage = sbase + st * S::STAGE;
@@ -325,25 +382,30 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
 }
 
 template <int KB, int NVB, int STAGES>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a, int mode, cudaStream_t stream) {
     using S = BwdCfg<KB, NVB, STAGES>;
     const uint32_t smem = S::BYTES + 1024;
     auto kern = kda_bwd_dh_kernel<KB, NVB, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int64_t ctas = (int64_t)a.N * a.H * (a.V / S::BV);
-    if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.dht,
-                                                       a.dhck, a.dv2, a.dh0, a.ws, a.L, a.scale, a.H, a.V);
+    const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
+    const int64_t ctas = (int64_t)a.N * a.H * (ncol / S::BV);
+    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    if (ctas <= 0 || segs <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)ctas, (unsigned)segs);
+    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.dht, a.dhck, a.dv2,
+                                             a.dh0, a.ws, a.L, a.scale, a.N, a.H, a.V, mode);
     return cudaGetLastError();
 }
 
 template <int KB>
-cudaError_t launch_bwd_k(const BwdArgs& a, cudaStream_t stream, int sms) {
-    const int64_t ctas64 = (int64_t)a.N * a.H * (a.V / 64);
-    if (ctas64 <= sms) return launch_bwd_t<KB, 1, 2>(a, stream);
-    if (a.V % 128 == 0) return launch_bwd_t<KB, 2, 2>(a, stream);
-    return launch_bwd_t<KB, 1, 1>(a, stream);
+cudaError_t launch_bwd_k(const BwdArgs& a, int mode, cudaStream_t stream, int sms) {
+    const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
+    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const int64_t ctas64 = (int64_t)a.N * a.H * (ncol / 64) * segs;
+    if (ctas64 <= sms) return launch_bwd_t<KB, 1, 2>(a, mode, stream);
+    if (ncol % 128 == 0) return launch_bwd_t<KB, 2, 2>(a, mode, stream);
+    return launch_bwd_t<KB, 1, 1>(a, mode, stream);
 }
 
 }  // namespace
@@ -353,9 +415,19 @@ cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         sms = 148;
-    if (a.K == 128) return launch_bwd_k<2>(a, stream, sms);
-    if (a.K == 64) return launch_bwd_k<1>(a, stream, sms);
-    return cudaErrorInvalidValue;
+    if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
+    auto run = [&](int mode) {
+        return a.K == 128 ? launch_bwd_k<2>(a, mode, stream, sms) : launch_bwd_k<1>(a, mode, stream, sms);
+    };
+    if (a.L.seg_count > 1) {
+        // segmented (the forward's plan): maps of every segment but the oldest,
+        // chained newest first from dht, then all segments in parallel
+        cudaError_t e = run(kScanModeMap);
+        if (e != cudaSuccess) return e;
+        e = launch_seg_combine(a.dht, a.ws, a.L, a.N, a.H, a.K, a.V, 0, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return run(kScanModeOutput);
 }
 
 }  // namespace kda

@@ -58,5 +58,8 @@ cudaError_t launch_plan(const int32_t* cu_seqlens, int N, int B, int T, uint8_t*
 cudaError_t launch_intra(const IntraArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream);
+// h_in[j+1] = P_j h_in[j] + Q_j over the segment maps in L.pq (h_in[0] = h0)
+cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, int N, int H, int K, int V,
+                               int flags, cudaStream_t stream);
 
 }  // namespace kda

@@ -611,6 +611,22 @@ cudaError_t launch_combine_k(const ScanArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, int N, int H, int K, int V,
+                               int flags, cudaStream_t stream) {
+    ScanArgs a{};
+    a.h0 = h0;
+    a.ws = ws;
+    a.L = L;
+    a.N = N;
+    a.H = H;
+    a.K = K;
+    a.V = V;
+    a.flags = flags;
+    if (K == 128) return launch_combine_k<128>(a, stream);
+    if (K == 64) return launch_combine_k<64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

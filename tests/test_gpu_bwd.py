@@ -213,3 +213,45 @@ def test_deterministic():
     b = run_bwd(x, gr)
     for u, w in zip(a, b):
         assert torch.equal(u, w)
+
+
+# ------------------------------------------------------------------ segmented reverse scan
+
+def _seg_plan(x):
+    import chunked_gated_delta_gb300 as kda
+    return kda.workspace_layout(_dims(x))
+
+
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 64), (128, 64), (64, 128)])
+def test_segmented_two_heads_ragged(K, V):
+    """Long sequence, few heads: maps of the newer segments, chained from dht,
+    then every segment in parallel."""
+    x = synth.make_inputs(make(B=1, T=64 * 100 + 17, H=2, K=K, V=V, seed=400 + K + V))
+    assert _seg_plan(x).seg_count >= 2
+    full_bwd_check(x, synth.make_bwd_inputs(x, seed=3), f"segmented K{K} V{V}")
+
+
+def test_segmented_varlen_uneven_and_empty():
+    lengths = [5000, 1, 0, 3000, 2048]
+    x = synth.make_inputs(make(T=0, H=2, seed=411), lengths=lengths)
+    assert _seg_plan(x).seg_count >= 2
+    gr = synth.make_bwd_inputs(x)
+    full_bwd_check(x, gr, "segmented varlen")
+    _, _, dh0 = run_bwd(x, gr)
+    torch.testing.assert_close(dh0[2].cpu(), gr["dht"][2], rtol=0, atol=0)  # empty sequence
+
+
+def test_segmented_no_dht():
+    x = synth.make_inputs(make(B=2, T=64 * 100 + 5, H=1, K=64, V=64, seed=421))
+    assert _seg_plan(x).seg_count >= 2
+    full_bwd_check(x, synth.make_bwd_inputs(x, dht=False), "segmented, dht None")
+
+
+def test_long_k64_workload_sampled():
+    x = synth.make_inputs(synth.WORKLOADS["long_k64"])
+    assert _seg_plan(x).seg_count >= 2
+    gr = synth.make_bwd_inputs(x)
+    units = sample_units(x, 2, seed=4, include=[(0, 0)])
+    gpu = run_bwd(x, gr)
+    res = compare_bwd(x, gpu, oracle_bwd(x, gr, units=units), units=units)
+    assert_bwd_within(res, "long_k64")
