@@ -218,22 +218,25 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             const int st = it % STAGES;
             const uint32_t sp = (it / STAGES) & 1;
             uint8_t* stage = sm + st * S::STAGE;
-            // checkpoint and MMA operand: dh before this chunk's update, bf16
+            // MMA operand: dh before this chunk's update, bf16
             if (has_row) {
-                uint4* ck = (dhck == nullptr || map_mode) ? nullptr
-                                            : reinterpret_cast<uint4*>(
-                                                  dhck + (((int64_t)(si.tile_base + c) * H + h) * K + r) * V + col);
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     const uint4 x = make_uint4(pack_bf16x2(dh[8 * cc], dh[8 * cc + 1]), pack_bf16x2(dh[8 * cc + 2], dh[8 * cc + 3]),
                                                pack_bf16x2(dh[8 * cc + 4], dh[8 * cc + 5]), pack_bf16x2(dh[8 * cc + 6], dh[8 * cc + 7]));
                     *reinterpret_cast<uint4*>(hs + r * 128 + ((cc ^ (r & 7)) << 4)) = x;
-                    if (ck) ck[cc] = x;
                 }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.h_ready);
+            // the checkpoint leaves after the hand-off (off the MMA's path), read
+            // back from the operand copy (the DV MMA only reads it too)
+            if (has_row && dhck != nullptr && !map_mode) {
+                uint4* ck = reinterpret_cast<uint4*>(dhck + (((int64_t)(si.tile_base + c) * H + h) * K + r) * V + col);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) ck[cc] = *reinterpret_cast<const uint4*>(hs + r * 128 + ((cc ^ (r & 7)) << 4));
+            }
             if (!wait(&B.full[st], sp)) break;
             if (quad < 2) {
                 // dv2[r, :] = DV[r, :] + dv_in[r, :], rows past the sequence end = 0
@@ -258,15 +261,18 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                         for (int t = 0; t < 4; ++t)
                             pw[t] = row_ok ? pack_bf16x2(dv[8 * hh + 2 * t] + bf_lo(iw[t]), dv[8 * hh + 2 * t + 1] + bf_hi(iw[t]))
                                            : 0u;
-                        const uint4 x = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                        *reinterpret_cast<uint4*>(vp + off) = x;
-                        if (row_ok && !map_mode) gdst[cc] = x;
+                        *reinterpret_cast<uint4*>(vp + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.vp_ready);
+                // dv2 rows leave after the hand-off, read back from the operand copy
+                if (row_ok && !map_mode) {
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) gdst[cc] = *reinterpret_cast<const uint4*>(vp + r * 128 + ((cc ^ (r & 7)) << 4));
+                }
             }
             const float decay = has_row ? ex2(reinterpret_cast<const float*>(stage + S::GD)[r]) : 0.f;
             if (!wait(&B.upd_full, it & 1)) break;
