@@ -255,3 +255,23 @@ def test_long_k64_workload_sampled():
     gpu = run_bwd(x, gr)
     res = compare_bwd(x, gpu, oracle_bwd(x, gr, units=units), units=units)
     assert_bwd_within(res, "long_k64")
+
+
+def test_grouped_value_heads():
+    """The reverse scan runs per value head on the forward's workspace, so
+    grouped q/k heads need nothing of it: compare with q/k expanded per value
+    head in the oracle."""
+    import chunked_gated_delta_gb300 as kda
+    x = synth.make_variant_inputs(make(B=1, T=300, H=4, seed=431), qk_heads=2)
+    gr = synth.make_bwd_inputs(x)
+    d, gd = to_dev(x), to_dev(gr)
+    dims = _dims(x)
+    ws = kda.new_workspace(dims, "cuda")
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"], workspace=ws)
+    gpu = kda.bwd_dh(x["scale"], gd["do"], gd["dv_in"], gd["dht"], dims, ws)
+    torch.cuda.synchronize()
+    xe = dict(x)
+    xe["q"] = x["q"].repeat_interleave(2, dim=2)
+    xe["k"] = x["k"].repeat_interleave(2, dim=2)
+    res = compare_bwd(x, gpu, oracle_bwd(xe, gr))
+    assert_bwd_within(res, "grouped heads")
