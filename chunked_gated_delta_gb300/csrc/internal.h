@@ -17,6 +17,8 @@ struct IntraArgs {
     WsLayout L;
     int H, K, V;                         // H = value heads
     int64_t max_chunks;
+    int beta_stride;                     // elements between beta rows (H, or more for a head group)
+    int beta_head0;                      // beta column of value head 0
     int f16;                             // q, k, v, beta are fp16 (else bf16)
     int flags;                           // kIntraBetaLogits
     int group;                           // value heads per q/k head

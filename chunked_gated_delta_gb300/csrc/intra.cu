@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap st_qg, const __grid_constant__ CUtensorMap st_w,
                      const __grid_constant__ CUtensorMap st_u, const uint16_t* __restrict__ beta,
-                     uint8_t* __restrict__ ws, const WsLayout L, const int H, const int flags, const int group) {
+                     uint8_t* __restrict__ ws, const WsLayout L, const int H, const int flags, const int group,
+                     const int beta_stride, const int beta_head0) {
     using S = IntraSmem<KB, VB>;
     constexpr int K = S::K, V = S::V, NCG = S::NCG, NSEG = S::NSEG, RS = S::RS;
     extern __shared__ uint8_t smem_raw[];
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
         const int i = tid - 64;
         float b = 0.f;
         if (i < valid) {
-            b = in_lo<F16>((uint32_t)beta[(int64_t)(row0 + i) * H + h]);
+            b = in_lo<F16>((uint32_t)beta[(int64_t)(row0 + i) * beta_stride + beta_head0 + h]);
             if (flags & kIntraBetaLogits) b = 1.f / (1.f + ex2(-b * kLog2e));  // sigmoid
         }
         beta_s[i] = b;
@@ -640,7 +641,8 @@ cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     const int64_t ctas = a.max_chunks * a.H;
     if (ctas <= 0) return cudaSuccess;
     kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_g, a.st_qg, a.st_w, a.st_u,
-                                                     a.beta, a.ws, a.L, a.H, a.flags, a.group);
+                                                     a.beta, a.ws, a.L, a.H, a.flags, a.group, a.beta_stride,
+                                                     a.beta_head0);
     return cudaGetLastError();
 }
 

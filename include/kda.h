@@ -195,6 +195,11 @@ kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const flo
  *   arena: device memory of at least kda_fwd_host_arena_size(dims) bytes,
  *   256-byte aligned, owned by the caller; it holds the device copies of the
  *   inputs and outputs and the workspace.
+ *   Problems of 4096 rows (B * T) or more with an even head count run as a
+ *   pipeline over two head groups: one group's host -> device copies overlap
+ *   the other's kernels and device -> host copies, on two streams the library
+ *   creates once per device (the call returns after enqueuing; `stream`
+ *   completes when every copy has).  Calls are serialised internally.
  */
 size_t kda_fwd_host_arena_size(const kda_dims* dims);
 kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float* g,

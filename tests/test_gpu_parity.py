@@ -272,3 +272,31 @@ def test_bounded_wait_expires_and_context_survives():
     o, ht = run_gpu(x)
     o_ref, ht_ref = oracle_ref(x)
     assert_within(compare(x, o, ht, o_ref, ht_ref), "after timeout self-check")
+
+
+@pytest.mark.parametrize("shape", ["fixed", "varlen"])
+def test_host_entry_point_head_group_pipeline(shape):
+    """Problems of 4096+ rows run kda_fwd_host as a pipeline over head groups
+    (copies of one group overlap the compute of the previous one): the result
+    matches the oracle and the device entry point."""
+    import chunked_gated_delta_gb300 as kda
+    if shape == "fixed":
+        x = synth.make_inputs(make(B=2, T=2100, H=8, seed=91))
+        x["h0"] = 0.1 * torch.randn((2, 8, 128, 128), generator=torch.Generator().manual_seed(4))
+    else:
+        x = synth.make_inputs(make(T=0, H=4, seed=92), lengths=[3000, 0, 1500, 77])
+    N = x["N"]
+    dims = kda.make_dims(x["B"], x["T"], x["H"], x["K"], x["V"], 0 if x["cu_seqlens"] is None else N)
+    arena = torch.empty(kda.host_arena_size(dims), dtype=torch.uint8, device="cuda")
+    pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    h0 = x["h0"].pin_memory() if x["h0"] is not None else None
+    cu = x["cu_seqlens"].pin_memory() if x["cu_seqlens"] is not None else None
+    o = torch.empty((x["B"], x["T"], x["H"], x["V"]), dtype=torch.bfloat16, pin_memory=True)
+    ht = torch.empty((N, x["H"], x["K"], x["V"]), dtype=torch.float32, pin_memory=True)
+    kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], x["scale"], h0, cu, o, ht, dims, arena)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = oracle_ref(x)
+    assert_within(compare(x, o, ht, o_ref, ht_ref), f"host pipeline {shape}")
+    o_dev, ht_dev = run_gpu(x)
+    torch.testing.assert_close(o.float(), o_dev.cpu().float(), rtol=2e-2, atol=2e-3)
+    torch.testing.assert_close(ht, ht_dev.cpu(), rtol=1e-2, atol=1e-3)
