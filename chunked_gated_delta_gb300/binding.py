@@ -25,7 +25,7 @@ STATUS_NAMES = {
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
            "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout", "kda_bwd_dh",
-           "kda_fwd_ex", "kda_fwd_intra_ex", "kda_fwd_scan_ex")
+           "kda_fwd_ex", "kda_fwd_intra_ex", "kda_fwd_scan_ex", "kda_bwd_dh_ex")
 
 
 class KdaError(RuntimeError):
@@ -94,6 +94,7 @@ def load_library(build_if_missing: bool = True):
             "kda_fwd_ex": (ctypes.c_int, [P, P, P, P, P, F32, P, P, P, P, D, O, P, SZ, P]),
             "kda_fwd_intra_ex": (ctypes.c_int, [P, P, P, P, P, P, D, O, P, SZ, P]),
             "kda_fwd_scan_ex": (ctypes.c_int, [F32, P, P, P, D, O, P, SZ, P]),
+            "kda_bwd_dh_ex": (ctypes.c_int, [F32, P, P, P, P, P, P, D, O, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -285,27 +286,38 @@ def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
     return int(load_library().kda_selftest_wait_timeout(_ptr(word), int(limit_ns), _stream_handle(stream)))
 
 
-def bwd_dh(scale, do, dv_in, dht, dims: Dims, workspace, want_dhck=True, want_dh0=True, stream=None):
-    """Reverse state scan on the GPU (kda_bwd_dh).  ``workspace`` must hold the
-    intra-chunk intermediates of the same inputs (from fwd / fwd_intra).
-    Returns (dhck [max_chunks,H,K,V] bf16 or None, dv2 [B,T,H,V] bf16,
-    dh0 [N,H,K,V] fp32 or None)."""
+def bwd_dh(scale, do, dv_in, dht, dims: Dims, workspace, want_dhck=True, want_dh0=True, stream=None,
+           state_dtype=None):
+    """Reverse state scan on the GPU (kda_bwd_dh_ex).  ``workspace`` must hold
+    the intra-chunk intermediates of the same inputs (from fwd / fwd_intra).
+    do, dv_in: [B,T,H,V] bf16 or fp16 (dv2 follows); dht: [N,H,K,V] fp32 or
+    bf16 or None (dh0 follows it, or ``state_dtype``).  Returns (dhck
+    [max_chunks,H,K,V] bf16 or None, dv2 [B,T,H,V], dh0 [N,H,K,V] or None)."""
     import torch
+    io = do.dtype
+    if io not in (torch.bfloat16, torch.float16):
+        raise TypeError("do must be bf16 or fp16")
     for name, t in (("do", do), ("dv_in", dv_in)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise TypeError(f"{name} must be a contiguous CUDA bf16 tensor")
-    if dht is not None and (dht.dtype != torch.float32 or not dht.is_cuda or not dht.is_contiguous()):
-        raise TypeError("dht must be a contiguous CUDA float32 tensor")
+        if t.dtype != io or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {io}")
+    if state_dtype is None:
+        state_dtype = dht.dtype if dht is not None else torch.float32
+    if state_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("the state dtype is float32 or bfloat16")
+    if dht is not None and (dht.dtype != state_dtype or not dht.is_cuda or not dht.is_contiguous()):
+        raise TypeError("dht must be a contiguous CUDA tensor of the state dtype")
     B, T, H, V = do.shape
     K = dims.K
     N = dims.num_seqs if dims.num_seqs > 0 else dims.B
     lay = workspace_layout(dims)
     dev = do.device
     dhck = torch.empty((lay.max_chunks, H, K, V), dtype=torch.bfloat16, device=dev) if want_dhck else None
-    dv2 = torch.zeros((B, T, H, V), dtype=torch.bfloat16, device=dev)
-    dh0 = torch.empty((N, H, K, V), dtype=torch.float32, device=dev) if want_dh0 else None
-    rc = load_library().kda_bwd_dh(float(scale), _ptr(do), _ptr(dv_in), _ptr(dht), _ptr(dhck), _ptr(dv2),
-                                   _ptr(dh0), ctypes.byref(dims), _ptr(workspace), workspace.numel(),
-                                   _stream_handle(stream))
-    _check(rc, "kda_bwd_dh")
+    dv2 = torch.zeros((B, T, H, V), dtype=io, device=dev)
+    dh0 = torch.empty((N, H, K, V), dtype=state_dtype, device=dev) if want_dh0 else None
+    opts = FwdOpts(IO_F16 if io == torch.float16 else IO_BF16,
+                   STATE_BF16 if state_dtype == torch.bfloat16 else STATE_F32, 0, 0)
+    rc = load_library().kda_bwd_dh_ex(float(scale), _ptr(do), _ptr(dv_in), _ptr(dht), _ptr(dhck), _ptr(dv2),
+                                      _ptr(dh0), ctypes.byref(dims), ctypes.byref(opts), _ptr(workspace),
+                                      workspace.numel(), _stream_handle(stream))
+    _check(rc, "kda_bwd_dh_ex")
     return dhck, dv2, dh0

@@ -37,6 +37,7 @@
 // from dht; the output pass runs all segments in parallel from their entry
 // gradients, each writing its own checkpoints and dv2 rows, the oldest dh0.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -53,6 +54,8 @@ __device__ __forceinline__ float ex2(float x) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
 __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -91,18 +94,19 @@ template <int STAGES>
 struct BwdBars {
     uint64_t full[STAGES], empty[STAGES];
     uint64_t h_ready, dv_full, vp_ready, upd_full;
+    uint64_t do_ready[STAGES];  // fp16 do converted to bf16 in the stage
     uint32_t tmem_slot;
     int abort_flag;
 };
 
-template <int KB, int NVB, int STAGES>
+template <int KB, int NVB, int STAGES, bool F16>
 __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, NVB, STAGES>::MIN_CTAS)
     kda_bwd_dh_kernel(const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_qg,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_dvin, const float* __restrict__ dht,
-                      uint16_t* __restrict__ dhck, uint16_t* __restrict__ dv2, float* __restrict__ dh0,
+                      const __grid_constant__ CUtensorMap tm_dvin, const void* __restrict__ dht,
+                      uint16_t* __restrict__ dhck, uint16_t* __restrict__ dv2, void* __restrict__ dh0,
                       uint8_t* __restrict__ ws, const WsLayout L, const float scale, const int N, const int H,
-                      const int V, const int mode) {
+                      const int V, const int mode, const int flags) {
     using S = BwdCfg<KB, NVB, STAGES>;
     constexpr int K = S::K;
     extern __shared__ uint8_t smem_raw[];
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
+    constexpr bool f16 = F16;  // do, dv_in, dv2 are fp16
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -146,6 +151,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         mbar_init(&B.dv_full, 1);
         mbar_init(&B.vp_ready, 2 * NVB);
         mbar_init(&B.upd_full, 1);
+        for (int i = 0; i < STAGES; ++i) mbar_init(&B.do_ready[i], 1);
         B.abort_flag = 0;
         fence_mbar_init();
     }
@@ -190,14 +196,29 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         // start: map mode [I | 0]; the newest segment dht (or 0); any other
         // segment the entry state the combine step chained for it
         const float* src_row = nullptr;
+        const bool dht_row = !map_mode && has_row && (seg == nseg - 1 || nseg == 0) && dht != nullptr;
         if (!map_mode && has_row) {
             if (seg == nseg - 1 || nseg == 0) {
-                if (dht != nullptr) src_row = dht + (((int64_t)s * H + h) * K + r) * V + col;
+                if (dht != nullptr && !(flags & kBwdStateBF16))
+                    src_row = static_cast<const float*>(dht) + (((int64_t)s * H + h) * K + r) * V + col;
             } else {
                 src_row = reinterpret_cast<const float*>(ws + L.hin) + ((((int64_t)rev * N + s) * H + h) * K + r) * V + col;
             }
         }
-        if (src_row != nullptr) {
+        if (dht_row && (flags & kBwdStateBF16)) {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dht) +
+                                                              (((int64_t)s * H + h) * K + r) * V + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 x = src[j];
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    dh[8 * j + 2 * t] = bf_lo(xw[t]);
+                    dh[8 * j + 2 * t + 1] = bf_hi(xw[t]);
+                }
+            }
+        } else if (src_row != nullptr) {
             const float4* src = reinterpret_cast<const float4*>(src_row);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -257,10 +278,24 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                         const uint4 iv = *reinterpret_cast<const uint4*>(stage + S::DVIN + vb * 8192 + off);
                         const uint32_t iw[4] = {iv.x, iv.y, iv.z, iv.w};
                         uint32_t pw[4];
+                        if constexpr (F16) {
+                            uint32_t ph[4];
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            pw[t] = row_ok ? pack_bf16x2(dv[8 * hh + 2 * t] + bf_lo(iw[t]), dv[8 * hh + 2 * t + 1] + bf_hi(iw[t]))
-                                           : 0u;
+                            for (int t = 0; t < 4; ++t) {
+                                const float x0 = dv[8 * hh + 2 * t] + h_lo(iw[t]);
+                                const float x1 = dv[8 * hh + 2 * t + 1] + h_hi(iw[t]);
+                                pw[t] = row_ok ? pack_bf16x2(x0, x1) : 0u;
+                                ph[t] = pack_f16x2(x0, x1);
+                            }
+                            // fp16 dv2 leaves from the fp32 values (the operand copy is bf16)
+                            if (row_ok && !map_mode) gdst[cc] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+                                pw[t] = row_ok ? pack_bf16x2(dv[8 * hh + 2 * t] + bf_lo(iw[t]),
+                                                             dv[8 * hh + 2 * t + 1] + bf_hi(iw[t]))
+                                               : 0u;
+                        }
                         *reinterpret_cast<uint4*>(vp + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                     }
                 }
@@ -269,7 +304,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.vp_ready);
                 // dv2 rows leave after the hand-off, read back from the operand copy
-                if (row_ok && !map_mode) {
+                if (row_ok && !map_mode && !f16) {
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) gdst[cc] = *reinterpret_cast<const uint4*>(vp + r * 128 + ((cc ^ (r & 7)) << 4));
                 }
@@ -298,18 +333,48 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
 #pragma unroll
             for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
         } else if (!map_mode && seg == 0 && dh0 != nullptr && has_row && !timed_out && !*abort_flag) {
-            float4* dst = reinterpret_cast<float4*>(dh0 + (((int64_t)s * H + h) * K + r) * V + col);
+            const int64_t hrow = (((int64_t)s * H + h) * K + r) * V + col;  // element offset of this row
+            if (flags & kBwdStateBF16) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dh0) + hrow);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_uint4(pack_bf16x2(dh[8 * j], dh[8 * j + 1]), pack_bf16x2(dh[8 * j + 2], dh[8 * j + 3]),
+                                        pack_bf16x2(dh[8 * j + 4], dh[8 * j + 5]), pack_bf16x2(dh[8 * j + 6], dh[8 * j + 7]));
+            } else {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dh0) + hrow);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dst[j] = make_float4(dh[4 * j], dh[4 * j + 1], dh[4 * j + 2], dh[4 * j + 3]);
+            }
         }
     } else if (warp == S::TMA_WARP) {
         // ================= TMA producer =================
-        if (lane == 0 && nit > 0) {
-            prefetch_tmap(&tm_kg);
-            prefetch_tmap(&tm_qg);
-            prefetch_tmap(&tm_w);
-            prefetch_tmap(&tm_do);
-            prefetch_tmap(&tm_dvin);
+        // fp16 do: once a chunk's tiles have landed, the warp rewrites its do
+        // tiles as bf16 in place (the qg^T @ do MMA takes bf16 operands)
+        auto convert_do = [&](int j) {
+            const int sj = j % STAGES;
+            const bool ok = wait(&B.full[sj], (j / STAGES) & 1);
+            __syncwarp();
+            if (!ok) return;
+            uint4* t = reinterpret_cast<uint4*>(sm + sj * S::STAGE + S::DO);
+            for (int e = lane; e < NVB * 512; e += 32) {
+                const int b = e >> 9;
+                if (map_mode && v0 + b * 64 < K) continue;  // P columns: zero tiles
+                const uint4 x = t[e];
+                t[e] = make_uint4(pack_bf16x2(h_lo(x.x), h_hi(x.x)), pack_bf16x2(h_lo(x.y), h_hi(x.y)),
+                                  pack_bf16x2(h_lo(x.z), h_hi(x.z)), pack_bf16x2(h_lo(x.w), h_hi(x.w)));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.do_ready[sj]);
+        };
+        if (nit > 0 && (F16 || lane == 0)) {  // bf16: lane 0 alone; fp16: the warp also converts do
+            if (lane == 0) {
+                prefetch_tmap(&tm_kg);
+                prefetch_tmap(&tm_qg);
+                prefetch_tmap(&tm_w);
+                prefetch_tmap(&tm_do);
+                prefetch_tmap(&tm_dvin);
+            }
             const float* gd = reinterpret_cast<const float*>(ws + L.gd);
             uint32_t tx = S::TX_BYTES;  // map mode: no do / dv_in for P columns
 #pragma unroll
@@ -319,28 +384,35 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 const int c = c_hi - 1 - it;
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
-                if (!wait(&B.empty[st], sp ^ 1)) break;
-                uint8_t* stage = sm + st * S::STAGE;
-                const int64_t tile = (int64_t)(si.tile_base + c) * H + h;
-                const int row = (int)(tile * 64);
-                const int trow = si.bos + c * 64;
-                uint64_t* fb = &B.full[st];
-                mbar_arrive_expect_tx(fb, tx);
+                bool issued = false;
+                if (lane == 0 && wait(&B.empty[st], sp ^ 1)) {  // lane 0 issues the copies
+                    issued = true;
+                    uint8_t* stage = sm + st * S::STAGE;
+                    const int64_t tile = (int64_t)(si.tile_base + c) * H + h;
+                    const int row = (int)(tile * 64);
+                    const int trow = si.bos + c * 64;
+                    uint64_t* fb = &B.full[st];
+                    mbar_arrive_expect_tx(fb, tx);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    tma_load_2d(stage + S::AKQ + kb * 16384, &tm_kg, fb, kb * 64, row);
-                    tma_load_2d(stage + S::AKQ + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
-                    tma_load_2d(stage + S::W + kb * 8192, &tm_w, fb, kb * 64, row);
-                }
+                    for (int kb = 0; kb < KB; ++kb) {
+                        tma_load_2d(stage + S::AKQ + kb * 16384, &tm_kg, fb, kb * 64, row);
+                        tma_load_2d(stage + S::AKQ + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
+                        tma_load_2d(stage + S::W + kb * 8192, &tm_w, fb, kb * 64, row);
+                    }
 #pragma unroll
-                for (int vb = 0; vb < NVB; ++vb) {
-                    const int cb = v0 + vb * 64, uc = map_mode ? cb - K : cb;  // column in the user tensors
-                    if (uc < 0) continue;
-                    tma_load_3d(stage + S::DO + vb * 8192, &tm_do, fb, uc, h, trow);
-                    tma_load_3d(stage + S::DVIN + vb * 8192, &tm_dvin, fb, uc, h, trow);
+                    for (int vb = 0; vb < NVB; ++vb) {
+                        const int cb = v0 + vb * 64, uc = map_mode ? cb - K : cb;  // column in the user tensors
+                        if (uc < 0) continue;
+                        tma_load_3d(stage + S::DO + vb * 8192, &tm_do, fb, uc, h, trow);
+                        tma_load_3d(stage + S::DVIN + vb * 8192, &tm_dvin, fb, uc, h, trow);
+                    }
+                    bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
                 }
-                bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
+                if constexpr (F16) issued = __shfl_sync(0xffffffffu, issued, 0);
+                if (!issued) break;
+                if (f16 && it >= 1) convert_do(it - 1);
             }
+            if (f16 && nit > 0 && !*abort_flag) convert_do(nit - 1);
         }
     } else if (warp == S::MMA_WARP) {
         // ================= tcgen05 issuer =================
@@ -362,6 +434,8 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 }
                 mma_commit(&B.dv_full);
                 // QD = qg^T @ do: the qg blocks sit 16 KB apart (K = 64: the next 8 KB are unused rows)
+                if (f16 && !wait(&B.do_ready[st], sp)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(t_qd, smem_desc(stage + S::AKQ + 8192 + ks * 2048, KB == 2 ? 16384 : 8192, 1024),
@@ -387,11 +461,11 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
     if (timed_out) atomicOr(status, kStatusTimeout);
 }
 
-template <int KB, int NVB, int STAGES>
-cudaError_t launch_bwd_t(const BwdArgs& a, int mode, cudaStream_t stream) {
+template <int KB, int NVB, int STAGES, bool F16>
+cudaError_t launch_bwd_f(const BwdArgs& a, int mode, cudaStream_t stream) {
     using S = BwdCfg<KB, NVB, STAGES>;
     const uint32_t smem = S::BYTES + 1024;
-    auto kern = kda_bwd_dh_kernel<KB, NVB, STAGES>;
+    auto kern = kda_bwd_dh_kernel<KB, NVB, STAGES, F16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
@@ -400,8 +474,14 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int mode, cudaStream_t stream) {
     if (ctas <= 0 || segs <= 0) return cudaSuccess;
     const dim3 grid((unsigned)ctas, (unsigned)segs);
     kern<<<grid, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.dht, a.dhck, a.dv2,
-                                             a.dh0, a.ws, a.L, a.scale, a.N, a.H, a.V, mode);
+                                             a.dh0, a.ws, a.L, a.scale, a.N, a.H, a.V, mode, a.flags);
     return cudaGetLastError();
+}
+
+template <int KB, int NVB, int STAGES>
+cudaError_t launch_bwd_t(const BwdArgs& a, int mode, cudaStream_t stream) {
+    return (a.flags & kBwdF16) ? launch_bwd_f<KB, NVB, STAGES, true>(a, mode, stream)
+                               : launch_bwd_f<KB, NVB, STAGES, false>(a, mode, stream);
 }
 
 template <int KB>
@@ -430,7 +510,8 @@ cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream) {
         // chained newest first from dht, then all segments in parallel
         cudaError_t e = run(kScanModeMap);
         if (e != cudaSuccess) return e;
-        e = launch_seg_combine(a.dht, a.ws, a.L, a.N, a.H, a.K, a.V, 0, stream);
+        e = launch_seg_combine(a.dht, a.ws, a.L, a.N, a.H, a.K, a.V, (a.flags & kBwdStateBF16) ? kScanStateBF16 : 0,
+                               stream);
         if (e != cudaSuccess) return e;
     }
     return run(kScanModeOutput);

@@ -45,15 +45,19 @@ struct ScanArgs {
 struct BwdArgs {
     CUtensorMap tm_kg, tm_qg, tm_w;  // workspace tiles, 2-D {dim, tiles*64}
     CUtensorMap tm_do, tm_dvin;      // user tensors, 3-D {V, H, rows}
-    const float* dht;   // [N, H, K, V] or null
+    const void* dht;    // fp32 (or bf16) [N, H, K, V] or null
     uint16_t* dhck;     // bf16 [chunks, H, K, V] or null
-    uint16_t* dv2;      // bf16 [rows, H, V]
-    float* dh0;         // [N, H, K, V] or null
+    uint16_t* dv2;      // bf16 (or fp16) [rows, H, V]
+    void* dh0;          // fp32 (or bf16) [N, H, K, V] or null
     uint8_t* ws;
     WsLayout L;
     float scale;
     int N, H, K, V;
+    int flags;          // kBwdF16 | kBwdStateBF16
 };
+
+constexpr int kBwdF16 = 1;         // do, dv_in, dv2 are fp16 (else bf16)
+constexpr int kBwdStateBF16 = 2;   // dht, dh0 are bf16 (else fp32)
 
 cudaError_t launch_plan(const int32_t* cu_seqlens, int N, int B, int T, uint8_t* ws,
                         const WsLayout& L, cudaStream_t stream);

@@ -317,9 +317,16 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
     return kda_fwd_scan_ex(scale, h0, o, ht, dims, nullptr, workspace, workspace_bytes, stream);
 }
 
-kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const float* dht, void* dhck, void* dv2,
-                      float* dh0, const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+kda_status kda_bwd_dh_ex(float scale, const void* do_, const void* dv_in, const void* dht, void* dhck, void* dv2,
+                         void* dh0, const kda_dims* dims, const kda_fwd_opts* opts, void* workspace,
+                         size_t workspace_bytes, void* stream) {
     if (!dims) return KDA_ERR_INVALID_ARG;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    if (op.io_dtype != KDA_IO_BF16 && op.io_dtype != KDA_IO_F16) return KDA_ERR_INVALID_ARG;
+    if (op.state_dtype != KDA_STATE_F32 && op.state_dtype != KDA_STATE_BF16) return KDA_ERR_INVALID_ARG;
+    const CUtensorMapDataType io =
+        op.io_dtype == KDA_IO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const bool varlen = is_varlen(dims);
     kda_status st = check_dims(dims, varlen);
     if (st != KDA_OK) return st;
@@ -338,10 +345,8 @@ kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const flo
         bool ok = map2(&a.tm_kg, ws + L.kg, dims->K, trows);
         ok = ok && map2(&a.tm_qg, ws + L.qg, dims->K, trows);
         ok = ok && map2(&a.tm_w, ws + L.w, dims->K, trows);
-        ok = ok && map3(&a.tm_do, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, do_, dims->V, dims->H, rows, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-        ok = ok && map3(&a.tm_dvin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dv_in, dims->V, dims->H, rows, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && map3(&a.tm_do, io, 2, do_, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && map3(&a.tm_dvin, io, 2, dv_in, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         if (!ok) return KDA_ERR_CUDA;
     }
     a.dht = dht;
@@ -355,8 +360,14 @@ kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const flo
     a.H = dims->H;
     a.K = dims->K;
     a.V = dims->V;
+    a.flags = (op.io_dtype == KDA_IO_F16 ? kBwdF16 : 0) | (op.state_dtype == KDA_STATE_BF16 ? kBwdStateBF16 : 0);
     if (launch_bwd_dh(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const float* dht, void* dhck, void* dv2,
+                      float* dh0, const kda_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+    return kda_bwd_dh_ex(scale, do_, dv_in, dht, dhck, dv2, dh0, dims, nullptr, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g, const void* beta,

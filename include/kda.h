@@ -160,6 +160,20 @@ kda_status kda_fwd_scan_ex(float scale, const void* h0, void* o, void* ht, const
                            void* stream);
 
 /*
+ * kda_bwd_dh with interface variants.  Of `opts` (NULL = kda_bwd_dh) the
+ * reverse scan reads io_dtype and state_dtype:
+ *   io_dtype     KDA_IO_F16: do, dv_in and dv2 are fp16 (do is rounded to bf16
+ *                on chip for the qg^T @ do product, whose other operand is the
+ *                bf16 qg; dv_in is added and dv2 written from fp32).
+ *   state_dtype  KDA_STATE_BF16: dht and dh0 are bf16 (dh is carried in fp32).
+ * The checkpoints dhck stay bf16.  beta_logits and qk_heads shaped the forward
+ * whose workspace this call reads; they are ignored here.
+ */
+kda_status kda_bwd_dh_ex(float scale, const void* do_, const void* dv_in, const void* dht, void* dhck,
+                         void* dv2, void* dh0, const kda_dims* dims, const kda_fwd_opts* opts,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Reverse state scan (the backward of the inter-chunk stage): the gradient of
  * the loss with respect to the recurrent state at every chunk boundary, after
  * kernel-fun "kda/_kernels/bwd_dhu.py".  With dh the gradient w.r.t. the state

@@ -275,3 +275,27 @@ def test_grouped_value_heads():
     xe["k"] = x["k"].repeat_interleave(2, dim=2)
     res = compare_bwd(x, gpu, oracle_bwd(xe, gr))
     assert_bwd_within(res, "grouped heads")
+
+
+
+# ------------------------------------------------------------------ interface variants
+
+@pytest.mark.parametrize("io,state", [(torch.float16, torch.float32), (torch.bfloat16, torch.bfloat16),
+                                      (torch.float16, torch.bfloat16)])
+@pytest.mark.parametrize("T", [130, 64 * 100 + 17])
+def test_f16_gradients_and_bf16_state(io, state, T):
+    """fp16 do / dv_in / dv2 and bf16 dht / dh0 (also through the segmented
+    path at the longer length), against the oracle on the exact input values."""
+    import chunked_gated_delta_gb300 as kda
+    x = synth.make_inputs(make(B=1, T=T, H=2, seed=440 + T))
+    gr = synth.make_bwd_inputs(x)
+    gr = {"do": gr["do"].float().to(io), "dv_in": gr["dv_in"].float().to(io), "dht": gr["dht"].to(state)}
+    d, gd = to_dev(x), to_dev(gr)
+    dims = _dims(x)
+    ws = kda.new_workspace(dims, "cuda")
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"], workspace=ws)
+    dhck, dv2, dh0 = kda.bwd_dh(x["scale"], gd["do"], gd["dv_in"], gd["dht"], dims, ws)
+    torch.cuda.synchronize()
+    assert dv2.dtype == io and dh0.dtype == state
+    res = compare_bwd(x, (dhck, dv2.float(), dh0.float()), oracle_bwd(x, gr))
+    assert_bwd_within(res, f"io {io} state {state} T {T}")

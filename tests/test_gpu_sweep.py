@@ -58,15 +58,15 @@ def test_forward_random_case(i):
 
 @pytest.mark.parametrize("i", range(0, N_CASES, 3))
 def test_reverse_scan_random_case(i):
-    """bf16 I/O cases of the sweep (the reverse scan takes bf16 gradients)."""
+    """Every third case of the sweep through the reverse scan, with gradients in
+    the case's io dtype and state in its state dtype."""
     from test_gpu_bwd import _dims, assert_bwd_within, compare_bwd, oracle_bwd
     x = _case(i)
-    if x["q"].dtype != torch.bfloat16:
-        pytest.skip("the reverse scan takes bf16 inputs")
-    if x["h0"] is not None and x["h0"].dtype != torch.float32:
-        x["h0"] = x["h0"].float()
     G = x["H"] // x["qk_heads"]
     gr = synth.make_bwd_inputs(x)
+    io = x["q"].dtype
+    state = x["h0"].dtype if x["h0"] is not None else torch.float32
+    gr = {"do": gr["do"].float().to(io), "dv_in": gr["dv_in"].float().to(io), "dht": gr["dht"].to(state)}
     d, gd = to_dev(x), to_dev(gr)
     dims = _dims(x)
     ws = kda.new_workspace(dims, "cuda")
@@ -79,5 +79,5 @@ def test_reverse_scan_random_case(i):
     xe["k"] = x["k"].repeat_interleave(G, dim=2)
     if x["beta_logits"]:
         xe["beta"] = torch.sigmoid(x["beta"].double())
-    res = compare_bwd(x, gpu, oracle_bwd(xe, gr))
+    res = compare_bwd(x, (gpu[0], gpu[1].float(), gpu[2].float()), oracle_bwd(xe, gr))
     assert_bwd_within(res, f"case {i}")
