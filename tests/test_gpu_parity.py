@@ -300,3 +300,22 @@ def test_host_entry_point_head_group_pipeline(shape):
     o_dev, ht_dev = run_gpu(x)
     torch.testing.assert_close(o.float(), o_dev.cpu().float(), rtol=2e-2, atol=2e-3)
     torch.testing.assert_close(ht, ht_dev.cpu(), rtol=1e-2, atol=1e-3)
+
+
+def test_varlen_thousands_of_short_sequences():
+    """3000 packed sequences of 0-20 tokens (plus a few long ones): the
+    planner's per-thread sequence ranges (more sequences than its threads),
+    one-chunk sequences everywhere, and empty ones keeping h0."""
+    rng = np.random.default_rng(77)
+    lengths = [int(v) for v in rng.integers(0, 21, size=3000)]
+    lengths[5] = 700
+    lengths[2999] = 129
+    x = synth.make_inputs(make(T=0, H=2, seed=97), lengths=lengths)
+    x["h0"] = 0.1 * torch.randn((len(lengths), 2, 128, 128), generator=torch.Generator().manual_seed(6))
+    o, ht = run_gpu(x)
+    units = sample_units(x, 40, seed=2, include=[(5, 0), (2999, 1)] + [(s, 0) for s in range(8)])
+    o_ref, ht_ref = oracle_ref(x, units=units)
+    assert_within(compare(x, o, ht, o_ref, ht_ref, units=units), "3000 sequences")
+    for s, n in enumerate(lengths):
+        if n == 0:
+            torch.testing.assert_close(ht[s].cpu(), x["h0"][s], rtol=0, atol=0)
