@@ -19,7 +19,9 @@
 //   warps 0..4*NVB-1   recurrence: thread r owns dh row r (fp32 registers) and,
 //                      in TMEM quadrants 0-1, token row r of dv2.
 //   next warp          TMA producer: kg, qg, w (workspace), do and dv_in (user
-//                      tensors) and gd per chunk into a STAGES-deep ring.
+//                      tensors) and gd per chunk into a STAGES-deep ring; with
+//                      fp16 gradients the warp also rewrites each landed do
+//                      tile as bf16 for the qg^T @ do product.
 //   next warp          tcgen05 issuer + TMEM owner.
 // MMAs, all M = 128:
 //   DV = [kg ; qg] @ dh      TMEM lanes 0-63 (rows 64-127 unused)

@@ -17,7 +17,8 @@
 //   w        = T' (k * exp2(g2)),   u = T' v         -> workspace
 //
 // GB300 mapping: 256 threads, ~73 KB of shared memory and 128 TMEM columns
-// per CTA, so three tiles are in flight on every SM.
+// per CTA, so three tiles are in flight on every SM (four at K = V = 64, whose
+// CTA needs 55 KB and fits in 64 registers per thread).
 //  * q, k, g arrive by TMA (3-D maps over [rows, H, dim]; q, k with a 128-byte
 //    swizzle, straight into the layouts the tensor core reads).  Each thread
 //    owns a block of 4 key dims x RS rows: it reads its g once into registers
