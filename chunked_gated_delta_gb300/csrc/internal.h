@@ -10,8 +10,9 @@
 namespace kda {
 
 struct IntraArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;      // user inputs, 3-D {dim, H, rows}
-    CUtensorMap st_qg, st_w, st_u, st_aqk;   // workspace tiles (stores), 2-D {dim, tiles*64}
+    CUtensorMap tm_q, tm_k, tm_v;            // user inputs, 3-D {dim, H, rows}
+    CUtensorMap st_qg, st_w, st_u;           // workspace tiles (stores), 2-D {dim, tiles*64}
+    const float* g;                      // fp32 [rows, H, K]
     const uint16_t* beta;                // bf16 or fp16 bits [rows, H]
     uint8_t* ws;
     WsLayout L;

@@ -16,18 +16,17 @@
 //   T        = (I + A)^-1,   T' = T diag(beta)
 //   w        = T' (k * exp2(g2)),   u = T' v         -> workspace
 //
-// GB300 mapping: 256 threads, ~73 KB of shared memory and 128 TMEM columns
-// per CTA, so three tiles are in flight on every SM (four at K = V = 64, whose
-// CTA needs 55 KB and fits in 64 registers per thread).
-//  * q, k, g arrive by TMA (3-D maps over [rows, H, dim]; q, k with a 128-byte
-//    swizzle, straight into the layouts the tensor core reads).  Each thread
-//    owns a block of 4 key dims x RS rows: it reads its g once into registers
-//    (pass 1, segment sums), then forms its g2 prefix from the segment sums
-//    and gates its q / k elements in place (pass 2) -- g2 never goes back to
-//    shared memory, and the g region is free after pass 1: it becomes the
-//    k exp2(-g2) operand and receives v by TMA while the gating runs.  Rows
-//    past the end of the sequence are zeroed on chip, so padding rows are
-//    inert.
+// GB300 mapping: 256 threads, 52 KB of shared memory, 128 TMEM columns and
+// 64 registers per thread, so four tiles are in flight on every SM (the SM's
+// 512 TMEM columns bound it there).
+//  * q, k (3-D maps over [rows, H, dim], 128-byte swizzle, straight into the
+//    layouts the tensor core reads) and, when it does not fit the q slots, v
+//    arrive by TMA.  g never enters shared memory: each thread owns a block of
+//    4 key dims x RS rows and reads it from global memory into registers with
+//    16-byte loads (one warp reads whole 512-byte rows), forms its segment sums
+//    (pass 1), then its g2 prefix from all segments' sums (pass 2), and gates
+//    its q / k elements in place.  Rows past the end of the sequence are
+//    zeroed on chip, so padding rows are inert.
 //  * Gated products use one gate factorisation, (q exp2(g2)) . (k exp2(-g2)),
 //    so Aqk and the k.k^T Gram matrix come out of ONE tcgen05 MMA with M = 128
 //    (A operand = [qg ; k exp2(g2)] stacked, B = k exp2(-g2)), accumulated in
@@ -37,17 +36,21 @@
 //    forward substitution, then the off-diagonal blocks level by level,
 //    T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ, as warp-level m16n8k8 tf32 MMAs
 //    with fp32 accumulation (16x16 products on the latency path, where a
-//    tcgen05 round trip would cost more than the math).
+//    tcgen05 round trip would cost more than the math).  A is strictly lower
+//    triangular and T unit lower triangular, so both live in ONE 64x64 fp32
+//    matrix: A^T in the strict upper triangle, T's strict lower triangle below
+//    it; T's unit diagonal and zero upper triangle are implied, never stored.
 //  * w and u are computed transposed, w^T = (k exp2(g2))^T T'^T and
 //    u^T = v^T T'^T: the key / value dim is the MMA's M = 128, so every TMEM
 //    lane holds real data, and 128 columns of TMEM suffice.
 //  * qg, w and u leave through TMA stores from swizzled shared memory; Aqk,
 //    kg and gd through direct stores.
-//  * Every buffer after the loads reuses a dead one: k exp2(-g2) and v take
-//    the g region after pass 1, A^T takes the k exp2(-g2) region once the
-//    Gram MMA has read it, T takes the qg slots once their store has read
-//    them, T' takes the A^T region, and the w / u staging take the T and v
-//    regions.
+//  * Shared memory, in order of use: the QK region holds q and k, gated in
+//    place into qg and k exp2(g2); the qg slots receive v once the qg store and
+//    the Gram MMA have read them (when V <= K), and finally the w staging; the
+//    k exp2(g2) slots take the u staging once the w MMA has read them.  The
+//    16 KB M region holds the segment sums, then k exp2(-g2), then A^T + T,
+//    then T' (bf16, rewritten in place).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -64,7 +67,7 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -110,52 +113,46 @@ __device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* 
     mma_tf32_16x8x8(d, ah, bh);
 }
 
-// fp32 64x64 matrices in shared memory, row-major with 64 floats per row and
-// an XOR of the column's 8-float group by (row & 3): row-contiguous accesses,
+// fp32 64x64 matrix in shared memory, row-major with 64 floats per row and an
+// XOR of the column's 8-float group by (row & 3): row-contiguous accesses,
 // float4 row reads and the 4-row x 8-column fragment reads of the MMAs are
-// all free of bank conflicts.  The 64 rows may live in two 8 KB halves.
+// all free of bank conflicts.  It holds A^T in its strict upper triangle and
+// T in its strict lower triangle.
 struct Mat64 {
-    float* lo;  // rows 0..31
-    float* hi;  // rows 32..63
-    __device__ __forceinline__ float* at(int r, int c) const {
-        return (r < 32 ? lo : hi) + (r & 31) * 64 + (c ^ ((r & 3) << 3));
+    float* p;
+    __device__ __forceinline__ float* at(int r, int c) const { return p + r * 64 + (c ^ ((r & 3) << 3)); }
+    // T[r][c] (unit lower triangular: the diagonal and the upper triangle are
+    // implied; the stored upper triangle is A^T)
+    __device__ __forceinline__ float t(int r, int c) const {
+        const float x = *at(r, c);
+        return r > c ? x : (r == c ? 1.f : 0.f);
     }
 };
 
 // Exact gated sums of a chunk whose decay span is too large for the factored
-// MMA (kept out of line so its registers do not weigh on the common path).
-// qk: the raw q / k tiles (per 64-dim block [q 8K | k 8K], SW128); g2s: g2 as
-// fp32 [64][K].  Writes Aqk (bf16, zero above the diagonal) to global memory
-// and beta_i * (k_i . k_j gated) for j < i into A^T, after every thread has
-// finished reading g2s (which A^T overwrites).
-template <int K, bool F16>
-__device__ __noinline__ void exact_gated_sums(const uint8_t* qk, float* g2s, const float* beta_s, int valid,
-                                              uint16_t* aqk_g, Mat64 AMT) {
+// MMA (kept out of line so its registers do not weigh on the common path),
+// accumulated over one 64-dim block of key dims: qk is the block's raw
+// [q 8K | k 8K] tiles (SW128), g2h its g2 as fp32 [64][64].  For this thread's
+// (i, j) pairs, ea += q_i . k_j gated (j <= i) and eb += k_i . k_j gated.
+template <bool F16>
+__device__ __noinline__ void exact_sums_block(const uint8_t* qk, const float* g2h, int valid, float* ea,
+                                              float* eb) {
     constexpr int kPairs = 64 * 64 / kThreads;
-    float sk[kPairs];
-#pragma unroll
     for (int n = 0; n < kPairs; ++n) {
         const int e = threadIdx.x + kThreads * n, i = e >> 6, j = e & 63;
-        float a = 0.f, b = 0.f;
         if (j <= i && i < valid) {
-            for (int d = 0; d < K; ++d) {
-                const uint8_t* qb = qk + (d >> 6) * 16384;
-                const float qi = in_at<F16>(qb + sw128_offset(i, d & 63));
-                const float ki = in_at<F16>(qb + 8192 + sw128_offset(i, d & 63));
-                const float kj = in_at<F16>(qb + 8192 + sw128_offset(j, d & 63));
-                const float gate = ex2(g2s[i * K + d] - g2s[j * K + d]);
+            float a = ea[n], b = eb[n];
+            for (int d = 0; d < 64; ++d) {
+                const float qi = in_at<F16>(qk + sw128_offset(i, d));
+                const float ki = in_at<F16>(qk + 8192 + sw128_offset(i, d));
+                const float kj = in_at<F16>(qk + 8192 + sw128_offset(j, d));
+                const float gate = ex2(g2h[i * 64 + d] - g2h[j * 64 + d]);
                 a = fmaf(qi * kj, gate, a);
                 b = fmaf(ki * kj, gate, b);
             }
+            ea[n] = a;
+            eb[n] = b;
         }
-        aqk_g[e] = bf16_bits(a);
-        sk[n] = (j < i) ? beta_s[i] * b : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int n = 0; n < kPairs; ++n) {
-        const int e = threadIdx.x + kThreads * n, i = e >> 6, j = e & 63;
-        *AMT.at(j, i) = sk[n];
     }
 }
 
@@ -165,47 +162,44 @@ struct IntraSmem {
     static constexpr int NCG = K / 4;             // 4-column groups
     static constexpr int NSEG = kThreads / NCG;   // row segments
     static constexpr int RS = 64 / NSEG;          // rows per segment
-    // QK: per kb [q / qg 8K | k / k*exp2(g2) 8K]; the qg slots later hold T, then w staging
+    // QK: per kb [q -> qg -> v block kb (V <= K) -> w staging 8K |
+    //             k -> k exp2(g2) -> u staging 8K]
     static constexpr uint32_t QK = 0;
-    // GV: g fp32 [64][K] (TMA); after pass 1: KI at GV (k*exp2(-g2), then A^T,
-    // then T') and v at GV + 16K (TMA), later the u staging
-    static constexpr uint32_t GV = QK + 2 * KB * 8192;
-    static constexpr uint32_t KI = GV;
-    static constexpr uint32_t VS = GV + 16384;
-    static constexpr uint32_t GV_BYTES = (64 * K * 4 > 16384 + VB * 8192) ? 64 * K * 4 : 16384 + VB * 8192;
-    // segment sums fp32 [NSEG][K] (cumsum passes only): own 4 KB when K = 128;
-    // when K = 64 they use the extra T region, which is free until the inverse
-    static constexpr uint32_t PART_OWN = GV + GV_BYTES;
-    static constexpr uint32_t XS = KB == 2 ? PART_OWN + NSEG * K * 4 : PART_OWN;  // X halves fp32 [6][16][8]
-    static constexpr uint32_t BETA = XS + 6 * 512;       // beta fp32 [64]
-    // rows 32..63 of T: the second qg slot when K = 128, an extra 8 KB when K = 64
-    static constexpr uint32_t TMHI = KB == 2 ? QK + 16384 : BETA + 256;
-    static constexpr uint32_t PART = KB == 2 ? PART_OWN : TMHI;
-    static constexpr uint32_t END = KB == 2 ? BETA + 256 : TMHI + 8192;
-    // the transposed w/u MMAs with K or V = 64 read 8 KB past their operand (unused rows)
-    static constexpr uint32_t BYTES = END > VS + 16384 ? END : VS + 16384;
-    static constexpr uint32_t QK_TX = 2 * KB * 8192, G_TX = 64 * K * 4, V_TX = VB * 8192;
+    // M (16 KB): segment sums fp32 [NSEG][K] -> k exp2(-g2) (KB x 8 KB) ->
+    // A^T + T fp32 [64][64] -> T' bf16 SW128 [64][64] (g2 blocks on the exact path)
+    static constexpr uint32_t M = QK + 2 * KB * 8192;
+    static constexpr uint32_t XS = M + 16384;     // X halves fp32 [6][16][8]
+    static constexpr uint32_t BETA = XS + 6 * 512;  // beta fp32 [64]
+    // v takes the qg slots (block vb at QK + 16 KB * vb) unless V > K
+    static constexpr bool V_OWN = VB > KB;
+    static constexpr uint32_t VS = V_OWN ? ((BETA + 256 + 1023) / 1024) * 1024 : QK;
+    static constexpr uint32_t VSTRIDE = V_OWN ? 8192 : 16384;
+    __device__ static constexpr uint32_t ustg(int vb) { return V_OWN ? VS + vb * 8192 : QK + vb * 16384 + 8192; }
+    // The transposed w / u MMAs with K or V = 64 read 8 KB past their operand
+    // (rows that land in unused TMEM lanes): QK + 16 KB .. + 24 KB, inside
+    // the allocation in every case.
+    static constexpr uint32_t BYTES = V_OWN ? VS + VB * 8192 : BETA + 256;
+    static constexpr uint32_t QK_TX = 2 * KB * 8192, V_TX = VB * 8192;
     static_assert(NSEG * K * 4 == 4096, "segment sums are 4 KB");
-    static_assert(KB == 2 || NSEG * K * 4 <= 8192, "segment sums fit the extra T region");
+    static_assert(BYTES >= 24576, "operand over-reads stay inside the allocation");
 };
 
 // flags: kIntraBetaLogits = beta holds logits (sigmoid applied here).
 // group: value heads per q/k head (value head h reads q/k head h / group).
-// Three CTAs per SM; four at K = V = 64 (55 KB of shared memory, 64 registers).
+// Four CTAs per SM (52 KB of shared memory, 64 registers, 128 TMEM columns).
 template <int KB, int VB, bool F16>
-__global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, 4)
     kda_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                     const __grid_constant__ CUtensorMap st_qg, const __grid_constant__ CUtensorMap st_w,
-                     const __grid_constant__ CUtensorMap st_u, const uint16_t* __restrict__ beta,
-                     uint8_t* __restrict__ ws, const WsLayout L, const int H, const int flags, const int group,
-                     const int beta_stride, const int beta_head0) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap st_qg,
+                     const __grid_constant__ CUtensorMap st_w, const __grid_constant__ CUtensorMap st_u,
+                     const float* __restrict__ g, const uint16_t* __restrict__ beta, uint8_t* __restrict__ ws,
+                     const WsLayout L, const int H, const int flags, const int group, const int beta_stride,
+                     const int beta_head0) {
     using S = IntraSmem<KB, VB>;
     constexpr int K = S::K, V = S::V, NCG = S::NCG, NSEG = S::NSEG, RS = S::RS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_qk, bar_g, bar_v, bar_mma;
+    uint8_t* sm = align_smem_1024(smem_raw);
+    __shared__ uint64_t bar_qk, bar_v, bar_mma;
     __shared__ uint32_t tmem_slot;
 
     const int64_t tile = blockIdx.x;  // chunk * H + head
@@ -218,25 +212,45 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
     const int valid = ci.valid, row0 = ci.row0;
     const int trow = static_cast<int>(tile * 64);  // first row of this tile in the workspace maps
     const uint32_t sbase = smem_u32(sm);
-    float* PARTs = reinterpret_cast<float*>(sm + S::PART);
+    float* PARTs = reinterpret_cast<float*>(sm + S::M);
     float* Xsm = reinterpret_cast<float*>(sm + S::XS);
     float* beta_s = reinterpret_cast<float*>(sm + S::BETA);
-    const Mat64 AMT{reinterpret_cast<float*>(sm + S::KI), reinterpret_cast<float*>(sm + S::KI + 8192)};
-    const Mat64 TM{reinterpret_cast<float*>(sm + S::QK), reinterpret_cast<float*>(sm + S::TMHI)};
+    const Mat64 PM{reinterpret_cast<float*>(sm + S::M)};
 
+    // ---- 0. this thread's g block [RS rows][4 dims] -> registers ------------
+    const int cg = tid % NCG, seg = tid / NCG;  // 4-column group, row segment
+    const int d0 = 4 * cg, kb_d = d0 >> 6, col = d0 & 63;
+    float gv[RS][4];
+    {
+        const float* gp = g + ((int64_t)row0 * H + h) * K + d0;
+        const int64_t rstride = (int64_t)H * K;
+#pragma unroll
+        for (int r = 0; r < RS; ++r) {
+            const int i = seg * RS + r;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < valid) x = ldg_stream_f4(gp + i * rstride);
+            gv[r][0] = x.x;
+            gv[r][1] = x.y;
+            gv[r][2] = x.z;
+            gv[r][3] = x.w;
+        }
+    }
     if (tid == 0) {
         mbar_init(&bar_qk, 1);
-        mbar_init(&bar_g, 1);
         mbar_init(&bar_v, 1);
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar_g, S::G_TX);
-        tma_load_3d(sm + S::GV, &tm_g, &bar_g, 0, h, row0);
         mbar_arrive_expect_tx(&bar_qk, S::QK_TX);
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) {
             tma_load_3d(sm + S::QK + kb * 16384, &tm_q, &bar_qk, kb * 64, h / group, row0);
             tma_load_3d(sm + S::QK + kb * 16384 + 8192, &tm_k, &bar_qk, kb * 64, h / group, row0);
+        }
+        if constexpr (S::V_OWN) {
+            mbar_arrive_expect_tx(&bar_v, S::V_TX);
+#pragma unroll
+            for (int vb = 0; vb < VB; ++vb)
+                tma_load_3d(sm + S::VS + vb * 8192, &tm_v, &bar_v, vb * 64, h, row0);
         }
     }
     if (warp == 0) {
@@ -252,38 +266,24 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
         }
         beta_s[i] = b;
     }
+
+    // ---- 1. pass 1: segment sums ---------------------------------------------
+    {
+        float4 sacc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < RS; ++r) {
+            sacc.x += gv[r][0];
+            sacc.y += gv[r][1];
+            sacc.z += gv[r][2];
+            sacc.w += gv[r][3];
+        }
+        *reinterpret_cast<float4*>(PARTs + seg * K + d0) = sacc;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     bool timed_out = false;
-    if (warp == 0 && !mbar_wait(&bar_g, 0, kWaitLimitNs)) timed_out = true;
-    __syncthreads();
-
-    // ---- 1. pass 1: this thread's g block -> registers; segment sums ---------
-    const int cg = tid % NCG, seg = tid / NCG;  // 4-column group, row segment
-    const int d0 = 4 * cg, kb_d = d0 >> 6, col = d0 & 63;
-    float gv[RS][4];
-    {
-        const float* G = reinterpret_cast<const float*>(sm + S::GV);
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int r = 0; r < RS; ++r) {
-            const int i = seg * RS + r;
-            float4 x = *reinterpret_cast<const float4*>(G + i * K + d0);
-            if (i >= valid) x = make_float4(0.f, 0.f, 0.f, 0.f);
-            gv[r][0] = x.x;
-            gv[r][1] = x.y;
-            gv[r][2] = x.z;
-            gv[r][3] = x.w;
-            s.x += x.x;
-            s.y += x.y;
-            s.z += x.z;
-            s.w += x.w;
-        }
-        *reinterpret_cast<float4*>(PARTs + seg * K + d0) = s;
-    }
-    __syncthreads();  // the g region is dead from here on
 
     // ---- 1'. pass 2: g2 prefix (log2 space), G, overflow guard ---------------
     float Gd[4], eG[4];
@@ -334,20 +334,30 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
 
     // ---- 1b. (rare) exact gated sums for chunks with extreme decay -----------
     if (exact_path) {
-        // g2 -> the (dead) g region as fp32 [64][K]
-        float* g2s = reinterpret_cast<float*>(sm + S::GV);
+        // one 64-dim block of g2 at a time in the M region (the segment sums
+        // are dead), fp32 [64][64]
+        constexpr int kPairs = 64 * 64 / kThreads;
+        float* g2h = reinterpret_cast<float*>(sm + S::M);
+        float ea[kPairs], eb[kPairs];
 #pragma unroll
-        for (int r = 0; r < RS; ++r)
-            *reinterpret_cast<float4*>(g2s + (seg * RS + r) * K + d0) =
-                make_float4(gv[r][0], gv[r][1], gv[r][2], gv[r][3]);
-        __syncthreads();
-        exact_gated_sums<K, F16>(sm + S::QK, g2s, beta_s, valid, aqk_g, AMT);
-    }
-    // v into its slot of the g region (free now); it is needed only by the u MMA
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_v, S::V_TX);
+        for (int n = 0; n < kPairs; ++n) ea[n] = eb[n] = 0.f;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (kb_d == kb) {
 #pragma unroll
-        for (int vb = 0; vb < VB; ++vb) tma_load_3d(sm + S::VS + vb * 8192, &tm_v, &bar_v, vb * 64, h, row0);
+                for (int r = 0; r < RS; ++r)
+                    *reinterpret_cast<float4*>(g2h + (seg * RS + r) * 64 + col) =
+                        make_float4(gv[r][0], gv[r][1], gv[r][2], gv[r][3]);
+            }
+            __syncthreads();
+            exact_sums_block<F16>(sm + S::QK + kb * 16384, g2h, valid, ea, eb);
+            __syncthreads();  // every read of this g2 block is done
+        }
+#pragma unroll
+        for (int n = 0; n < kPairs; ++n) {
+            const int e = tid + kThreads * n, i = e >> 6, j = e & 63;
+            aqk_g[e] = bf16_bits(ea[n]);  // zero above the diagonal
+            if (j < i) *PM.at(j, i) = beta_s[i] * eb[n];
+        }
     }
 
     // ---- 2. gate this thread's q / k block in place; kg to global ------------
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
             *reinterpret_cast<uint2*>(qs + 8192 + off) =
                 make_uint2(pack_bf16x2(kga4[0], kga4[1]), pack_bf16x2(kga4[2], kga4[3]));
             if (!exact_path)
-                *reinterpret_cast<uint2*>(sm + S::KI + kb_d * 8192 + off) =
+                *reinterpret_cast<uint2*>(sm + S::M + kb_d * 8192 + off) =
                     make_uint2(pack_bf16x2(kin4[0], kin4[1]), pack_bf16x2(kin4[2], kin4[3]));
             *reinterpret_cast<uint2*>(kg_g + i * K) = make_uint2(pack_bf16x2(kg4[0], kg4[1]), pack_bf16x2(kg4[2], kg4[3]));
         }
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
                 for (int ks = 0; ks < K / 16; ++ks) {
                     const int kb = ks >> 2, kk = ks & 3;
                     const uint64_t ad = smem_desc(sbase + S::QK + kb * 16384 + kk * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(sbase + S::KI + kb * 8192 + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(sbase + S::M + kb * 8192 + kk * 32, 16, 1024);
                     mma_bf16(tmem, ad, bd, id, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_mma);
@@ -439,21 +449,32 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
                     dst[cc] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             } else {
-                // rows of k.k -> A^T (strictly lower A, beta on the row); the Gram
-                // MMA has finished reading k exp2(-g2) from KI
+                // rows of k.k -> A^T, the strict upper triangle of M (A is
+                // strictly lower, beta on the row); the Gram MMA has finished
+                // reading k exp2(-g2) from M
                 const int i = (quad - 2) * 32 + lane;
                 const float b = beta_s[i];
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     const int j = c0 + t;
-                    *AMT.at(j, i) = (j < i) ? b * r[t] : 0.f;
+                    if (j < i) *PM.at(j, i) = b * r[t];
                 }
             }
         }
     }
-    if (tid == 0) bulk_wait_read0();  // the qg store has read the qg slots that T takes over
+    if (tid == 0) {
+        bulk_wait_read0();  // the qg store has read the qg slots
+        if constexpr (!S::V_OWN) {
+            // v into the qg slots (the Gram MMA has read them too); it is
+            // needed only by the u MMA, after the inverse
+            mbar_arrive_expect_tx(&bar_v, S::V_TX);
+#pragma unroll
+            for (int vb = 0; vb < VB; ++vb)
+                tma_load_3d(sm + S::VS + vb * S::VSTRIDE, &tm_v, &bar_v, vb * 64, h, row0);
+        }
+    }
     __syncthreads();
-    // ---- 4. T = (I + A)^-1 by 16x16 blocks, fp32 ------------------------------
+    // ---- 4. T = (I + A)^-1 by 16x16 blocks, fp32, into M's strict lower triangle
     // level 0: diagonal blocks by forward substitution (column per thread)
     if (tid < 64) {
         const int I = tid >> 4, cc = tid & 15, b0 = 16 * I;
@@ -465,16 +486,18 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
             const float tm = acc[m];
 #pragma unroll
             for (int r4 = ((m + 1) / 4) * 4; r4 < 16; r4 += 4) {
-                // A[b0 + r][b0 + m] for r = r4..r4+3 (zero for r <= m): one float4 of A^T row b0 + m
-                const float4 a = *reinterpret_cast<const float4*>(AMT.at(b0 + m, b0 + r4));
-                acc[r4 + 0] = fmaf(-a.x, tm, acc[r4 + 0]);
-                acc[r4 + 1] = fmaf(-a.y, tm, acc[r4 + 1]);
-                acc[r4 + 2] = fmaf(-a.z, tm, acc[r4 + 2]);
+                // A[b0 + r][b0 + m] for r = r4..r4+3: one float4 of A^T row b0 + m;
+                // only r > m is A (the rest is T's storage)
+                const float4 a = *reinterpret_cast<const float4*>(PM.at(b0 + m, b0 + r4));
+                if (r4 + 0 > m) acc[r4 + 0] = fmaf(-a.x, tm, acc[r4 + 0]);
+                if (r4 + 1 > m) acc[r4 + 1] = fmaf(-a.y, tm, acc[r4 + 1]);
+                if (r4 + 2 > m) acc[r4 + 2] = fmaf(-a.z, tm, acc[r4 + 2]);
                 acc[r4 + 3] = fmaf(-a.w, tm, acc[r4 + 3]);
             }
         }
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) *TM.at(b0 + rr, b0 + cc) = acc[rr];
+        for (int rr = 1; rr < 16; ++rr)
+            if (rr > cc) *PM.at(b0 + rr, b0 + cc) = acc[rr];
     }
     __syncthreads();
     // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev.  One warp per
@@ -492,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const int kc = 16 * Kb + 8 * ks;
-                        const float a[4] = {*AMT.at(kc + t, 16 * I + gq), *AMT.at(kc + t, 16 * I + gq + 8),
-                                            *AMT.at(kc + t + 4, 16 * I + gq), *AMT.at(kc + t + 4, 16 * I + gq + 8)};
-                        const float b[2] = {*TM.at(kc + t, n0 + gq), *TM.at(kc + t + 4, n0 + gq)};
+                        const float a[4] = {*PM.at(kc + t, 16 * I + gq), *PM.at(kc + t, 16 * I + gq + 8),
+                                            *PM.at(kc + t + 4, 16 * I + gq), *PM.at(kc + t + 4, 16 * I + gq + 8)};
+                        const float b[2] = {PM.t(kc + t, n0 + gq), PM.t(kc + t + 4, n0 + gq)};
                         mma_tf32(acc, a, b);
                     }
                 }
@@ -507,33 +530,43 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const int kc = 16 * I + 8 * ks;
-                    const float a[4] = {*TM.at(16 * I + gq, kc + t), *TM.at(16 * I + gq + 8, kc + t),
-                                        *TM.at(16 * I + gq, kc + t + 4), *TM.at(16 * I + gq + 8, kc + t + 4)};
+                    const float a[4] = {PM.t(16 * I + gq, kc + t), PM.t(16 * I + gq + 8, kc + t),
+                                        PM.t(16 * I + gq, kc + t + 4), PM.t(16 * I + gq + 8, kc + t + 4)};
                     const float b[2] = {xw[(8 * ks + t) * 8 + gq], xw[(8 * ks + t + 4) * 8 + gq]};
                     mma_tf32(d, a, b);
                 }
-                *reinterpret_cast<float2*>(TM.at(16 * I + gq, n0 + 2 * t)) = make_float2(-d[0], -d[1]);
-                *reinterpret_cast<float2*>(TM.at(16 * I + gq + 8, n0 + 2 * t)) = make_float2(-d[2], -d[3]);
+                *reinterpret_cast<float2*>(PM.at(16 * I + gq, n0 + 2 * t)) = make_float2(-d[0], -d[1]);
+                *reinterpret_cast<float2*>(PM.at(16 * I + gq + 8, n0 + 2 * t)) = make_float2(-d[2], -d[3]);
                 __syncwarp();
             }
             __syncthreads();
         }
     }
-    // T' = T diag(beta) -> bf16, K-major SW128 [64 i][64 j] into KI (A^T is dead)
+    // T' = T diag(beta) -> bf16, K-major SW128 [64 i][64 j], written over M once
+    // every thread has read its part of T
     {
         const int i = tid >> 2, j0 = (tid & 3) * 16;
+        uint4 x[2];
 #pragma unroll
         for (int q8 = 0; q8 < 2; ++q8) {
             const int j = j0 + 8 * q8;
-            const float4 ta = *reinterpret_cast<const float4*>(TM.at(i, j));
-            const float4 tb = *reinterpret_cast<const float4*>(TM.at(i, j + 4));
+            const float4 ta = *reinterpret_cast<const float4*>(PM.at(i, j));
+            const float4 tb = *reinterpret_cast<const float4*>(PM.at(i, j + 4));
             const float4 ba = *reinterpret_cast<const float4*>(beta_s + j);
             const float4 bb = *reinterpret_cast<const float4*>(beta_s + j + 4);
-            const uint4 x = make_uint4(pack_bf16x2(j <= i ? ta.x * ba.x : 0.f, j + 1 <= i ? ta.y * ba.y : 0.f),
-                                       pack_bf16x2(j + 2 <= i ? ta.z * ba.z : 0.f, j + 3 <= i ? ta.w * ba.w : 0.f),
-                                       pack_bf16x2(j + 4 <= i ? tb.x * bb.x : 0.f, j + 5 <= i ? tb.y * bb.y : 0.f),
-                                       pack_bf16x2(j + 6 <= i ? tb.z * bb.z : 0.f, j + 7 <= i ? tb.w * bb.w : 0.f));
-            *reinterpret_cast<uint4*>(sm + S::KI + i * 128 + (((j >> 3) ^ (i & 7)) << 4)) = x;
+            const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+            const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = j + e < i ? tv[e] * bv[e] : (j + e == i ? bv[e] : 0.f);
+            x[q8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                               pack_bf16x2(y[6], y[7]));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q8 = 0; q8 < 2; ++q8) {
+            const int j = j0 + 8 * q8;
+            *reinterpret_cast<uint4*>(sm + S::M + i * 128 + (((j >> 3) ^ (i & 7)) << 4)) = x[q8];
         }
     }
     fence_proxy_async_smem();
@@ -548,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
         // past the end -> 0
         for (int e = tid; e < 64 * 8 * VB; e += kThreads) {
             const int rr = e / (8 * VB), x = e % (8 * VB);
-            uint4* p = reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * 8192 + rr * 128 + (x & 7) * 16);
+            uint4* p = reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * S::VSTRIDE + rr * 128 + (x & 7) * 16);
             uint4 y = make_uint4(0u, 0u, 0u, 0u);
             if (rr < valid) {
                 const uint4 hv = *p;
@@ -562,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
     } else {
         for (int e = tid; e < (64 - valid) * 8 * VB; e += kThreads) {  // zero v rows past the end
             const int rr = valid + e / (8 * VB), x = e % (8 * VB);
-            *reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * 8192 + rr * 128 + (x & 7) * 16) =
+            *reinterpret_cast<uint4*>(sm + S::VS + (x >> 3) * S::VSTRIDE + rr * 128 + (x & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -573,14 +606,16 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
         if (lane == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16_f32(128, 64, 1, 0);  // A MN-major, B K-major
-            // For K or V = 64 the second 64 rows of M read the next 8 KB of
-            // shared memory (rows that land in unused TMEM lanes).
+            // For K or V = 64 the second 64 rows of the MMA's M read the
+            // 8 KB one block stride further on (rows that land in unused TMEM
+            // lanes).
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = smem_desc(sbase + S::KI + ks * 32, 16, 1024);
+                const uint64_t bd = smem_desc(sbase + S::M + ks * 32, 16, 1024);
                 mma_bf16(tmem, smem_desc(sbase + S::QK + 8192 + ks * 2048, KB == 2 ? 16384 : 8192, 1024), bd, id,
                          ks > 0 ? 1u : 0u);
-                mma_bf16(tmem + 64, smem_desc(sbase + S::VS + ks * 2048, 8192, 1024), bd, id, ks > 0 ? 1u : 0u);
+                mma_bf16(tmem + 64, smem_desc(sbase + S::VS + ks * 2048, S::VSTRIDE, 1024), bd, id,
+                         ks > 0 ? 1u : 0u);
             }
             mma_commit(&bar_mma);
         }
@@ -599,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
             tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + i0, r);
             tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + i0 + 16, r + 16);
             tmem_ld_wait();
-            uint8_t* stg = sm + S::QK + (d >> 6) * 16384;  // the qg slots (T is dead)
+            uint8_t* stg = sm + S::QK + (d >> 6) * 16384;  // the qg slots (v is dead)
 #pragma unroll
             for (int t = 0; t < 32; ++t)
                 *reinterpret_cast<uint16_t*>(stg + sw128_offset(i0 + t, d & 63)) = bf16_bits(r[t]);
@@ -608,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
             tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 64 + i0, r);
             tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 64 + i0 + 16, r + 16);
             tmem_ld_wait();
-            uint8_t* stg = sm + S::VS + (d >> 6) * 8192;  // v is dead
+            uint8_t* stg = sm + S::ustg(d >> 6);  // k exp2(g2) (or v) is dead
 #pragma unroll
             for (int t = 0; t < 32; ++t)
                 *reinterpret_cast<uint16_t*>(stg + sw128_offset(i0 + t, d & 63)) = bf16_bits(r[t]);
@@ -621,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, KB == 1 && VB == 1 ? 4 : 3)
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) tma_store_2d(&st_w, sm + S::QK + kb * 16384, kb * 64, trow);
 #pragma unroll
-        for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::VS + vb * 8192, vb * 64, trow);
+        for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::ustg(vb), vb * 64, trow);
         bulk_commit();
         bulk_wait_read0();  // smem must outlive the reads; the writes complete with the grid
     }
@@ -639,9 +674,12 @@ cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     auto kern = kda_intra_kernel<KB, VB, F16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // four CTAs per SM need the largest shared-memory carveout
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     const int64_t ctas = a.max_chunks * a.H;
     if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_g, a.st_qg, a.st_w, a.st_u,
+    kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.st_qg, a.st_w, a.st_u, a.g,
                                                      a.beta, a.ws, a.L, a.H, a.flags, a.group, a.beta_stride,
                                                      a.beta_head0);
     return cudaGetLastError();

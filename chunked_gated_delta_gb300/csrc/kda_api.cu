@@ -229,14 +229,12 @@ kda_status intra_impl(const void* q, const void* k, const void* v, const float* 
     bool ok = map3(&a.tm_q, io, 2, q, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && map3(&a.tm_k, io, 2, k, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && map3(&a.tm_v, io, 2, v, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && map3(&a.tm_g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g, dims->K, dims->H, rows,
-                    (uint32_t)dims->K, CU_TENSOR_MAP_SWIZZLE_NONE);
     const int64_t trows = L.max_chunks * dims->H * kChunk;
     ok = ok && map2(&a.st_qg, ws + L.qg, dims->K, trows);
     ok = ok && map2(&a.st_w, ws + L.w, dims->K, trows);
     ok = ok && map2(&a.st_u, ws + L.u, dims->V, trows);
-    ok = ok && map2(&a.st_aqk, ws + L.aqk, kChunk, trows);
     if (!ok) return KDA_ERR_CUDA;
+    a.g = g;
     a.beta = static_cast<const uint16_t*>(beta);
     a.ws = ws;
     a.L = L;
