@@ -39,7 +39,9 @@
 //    tcgen05 round trip would cost more than the math).  A is strictly lower
 //    triangular and T unit lower triangular, so both live in ONE 64x64 fp32
 //    matrix: A^T in the strict upper triangle, T's strict lower triangle below
-//    it; T's unit diagonal and zero upper triangle are implied, never stored.
+//    it.  Once the substitution has consumed A's diagonal blocks, T's diagonal
+//    blocks are stored whole (unit diagonal, zeros above), so the later
+//    products read T without masks.
 //  * w and u are computed transposed, w^T = (k exp2(g2))^T T'^T and
 //    u^T = v^T T'^T: the key / value dim is the MMA's M = 128, so every TMEM
 //    lane holds real data, and 128 columns of TMEM suffice.
@@ -117,16 +119,11 @@ __device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* 
 // XOR of the column's 8-float group by (row & 3): row-contiguous accesses,
 // float4 row reads and the 4-row x 8-column fragment reads of the MMAs are
 // all free of bank conflicts.  It holds A^T in its strict upper triangle and
-// T in its strict lower triangle.
+// T in its strict lower triangle (T's diagonal 16x16 blocks whole, once A's
+// have been consumed).
 struct Mat64 {
     float* p;
     __device__ __forceinline__ float* at(int r, int c) const { return p + r * 64 + (c ^ ((r & 3) << 3)); }
-    // T[r][c] (unit lower triangular: the diagonal and the upper triangle are
-    // implied; the stored upper triangle is A^T)
-    __device__ __forceinline__ float t(int r, int c) const {
-        const float x = *at(r, c);
-        return r > c ? x : (r == c ? 1.f : 0.f);
-    }
 };
 
 // Exact gated sums of a chunk whose decay span is too large for the factored
@@ -495,9 +492,11 @@ __global__ void __launch_bounds__(kThreads, 4)
                 acc[r4 + 3] = fmaf(-a.w, tm, acc[r4 + 3]);
             }
         }
+        // acc is column cc of T_II whole (1 on the diagonal, 0 above it); it
+        // replaces A's diagonal block once every column's substitution is done
+        asm volatile("bar.sync 1, 64;" ::: "memory");
 #pragma unroll
-        for (int rr = 1; rr < 16; ++rr)
-            if (rr > cc) *PM.at(b0 + rr, b0 + cc) = acc[rr];
+        for (int rr = 0; rr < 16; ++rr) *PM.at(b0 + rr, b0 + cc) = acc[rr];
     }
     __syncthreads();
     // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev.  One warp per
@@ -517,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                         const int kc = 16 * Kb + 8 * ks;
                         const float a[4] = {*PM.at(kc + t, 16 * I + gq), *PM.at(kc + t, 16 * I + gq + 8),
                                             *PM.at(kc + t + 4, 16 * I + gq), *PM.at(kc + t + 4, 16 * I + gq + 8)};
-                        const float b[2] = {PM.t(kc + t, n0 + gq), PM.t(kc + t + 4, n0 + gq)};
+                        const float b[2] = {*PM.at(kc + t, n0 + gq), *PM.at(kc + t + 4, n0 + gq)};
                         mma_tf32(acc, a, b);
                     }
                 }
@@ -530,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const int kc = 16 * I + 8 * ks;
-                    const float a[4] = {PM.t(16 * I + gq, kc + t), PM.t(16 * I + gq + 8, kc + t),
-                                        PM.t(16 * I + gq, kc + t + 4), PM.t(16 * I + gq + 8, kc + t + 4)};
+                    const float a[4] = {*PM.at(16 * I + gq, kc + t), *PM.at(16 * I + gq + 8, kc + t),
+                                        *PM.at(16 * I + gq, kc + t + 4), *PM.at(16 * I + gq + 8, kc + t + 4)};
                     const float b[2] = {xw[(8 * ks + t) * 8 + gq], xw[(8 * ks + t + 4) * 8 + gq]};
                     mma_tf32(d, a, b);
                 }
@@ -558,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
             float y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = j + e < i ? tv[e] * bv[e] : (j + e == i ? bv[e] : 0.f);
+            for (int e = 0; e < 8; ++e) y[e] = j + e <= i ? tv[e] * bv[e] : 0.f;
             x[q8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                                pack_bf16x2(y[6], y[7]));
         }
@@ -625,28 +624,33 @@ __global__ void __launch_bounds__(kThreads, 4)
     __syncthreads();
     tc_fence_after();
 
-    // ---- 6. w^T / u^T columns -> swizzled [i][dim] staging -> TMA stores -------
+    // ---- 6. w^T / u^T -> swizzled [i][dim] staging -> TMA stores -------------
+    // Each warp reads 16-lane (dim) x 32-column (token) blocks in the m16n8
+    // fragment layout and writes them transposed, 8x8 bf16 matrices at a time.
     {
         const int quad = warp & 3, i0 = (warp >> 2) * 32;  // TMEM lane quadrant, token-row half
-        const int d = quad * 32 + lane;                     // TMEM lane = key dim (w) / value dim (u)
-        float r[32];
-        if (d < K) {
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + i0, r);
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + i0 + 16, r + 16);
-            tmem_ld_wait();
-            uint8_t* stg = sm + S::QK + (d >> 6) * 16384;  // the qg slots (v is dead)
+        const int mat = lane >> 3, mrow = lane & 7;         // the stmatrix row this lane addresses
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-                *reinterpret_cast<uint16_t*>(stg + sw128_offset(i0 + t, d & 63)) = bf16_bits(r[t]);
-        }
-        if (d < V) {
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 64 + i0, r);
-            tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 64 + i0 + 16, r + 16);
-            tmem_ld_wait();
-            uint8_t* stg = sm + S::ustg(d >> 6);  // k exp2(g2) (or v) is dead
+        for (int half = 0; half < 2; ++half) {
+            const int L0 = quad * 32 + half * 16;  // dims L0 .. L0 + 15
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-                *reinterpret_cast<uint16_t*>(stg + sw128_offset(i0 + t, d & 63)) = bf16_bits(r[t]);
+            for (int wu = 0; wu < 2; ++wu) {        // 0: w (columns i0..), 1: u (columns 64 + i0..)
+                if (L0 >= (wu == 0 ? K : V)) continue;
+                uint32_t r[16];
+                tmem_ld16x256_x4(tmem + ((uint32_t)L0 << 16) + wu * 64 + i0, r);
+                tmem_ld_wait();
+                const uint32_t stg = sbase + (wu == 0 ? S::QK + (L0 >> 6) * 16384 : S::ustg(L0 >> 6));
+#pragma unroll
+                for (int g2 = 0; g2 < 2; ++g2) {
+                    // matrices: 0 = dims L0.., tokens i0 + 16 g2 ..; 1 = dims L0 + 8..;
+                    // 2 and 3 the same for the next 8 tokens
+                    const float* f = reinterpret_cast<const float*>(r) + 8 * g2;
+                    const int tok = i0 + 16 * g2 + 8 * (mat >> 1) + mrow;
+                    const int dim = (L0 & 63) + 8 * (mat & 1);
+                    stmatrix_x4_trans(stg + sw128_offset(tok, dim), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                }
+            }
         }
     }
     fence_proxy_async_smem();

@@ -181,6 +181,27 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* r) {
                    "=r"(u[7])
                  : "r"(taddr));
 }
+// 16 lanes x 256 bits, 4 repetitions along the columns: for repetition g,
+// thread t gets u[4g + 0..1] = lane (base + t/4), columns col + 8g + 2(t%4) + {0, 1}
+// and u[4g + 2..3] = lane (base + 8 + t/4), the same columns (the layout of an
+// m16n8 mma accumulator fragment).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t* u) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+}
+// Four 8x8 b16 matrices stored transposed: register k of thread t holds row t/4,
+// columns 2(t%4), 2(t%4)+1 of matrix k, and threads 8k..8k+7 give the shared
+// addresses of the 8 (16-byte) rows of matrix k's transpose.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                  uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
