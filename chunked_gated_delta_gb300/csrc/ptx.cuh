@@ -221,11 +221,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 }
 
 // Instruction descriptor, .kind::f16 with bf16 A/B and fp32 D.
-// a_mn / b_mn: operand is MN-major (1) or K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+// a_mn / b_mn: operand is MN-major (1) or K-major (0); neg_a: D (+)= (-A) B.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn, int neg_a = 0) {
     return (1u << 4)                         // D format: f32
            | (1u << 7)                       // A format: bf16
            | (1u << 10)                      // B format: bf16
+           | ((uint32_t)neg_a << 13)         // negate A
            | ((uint32_t)a_mn << 15)          // A major
            | ((uint32_t)b_mn << 16)          // B major
            | ((uint32_t)(N >> 3) << 17)      // N / 8

@@ -18,9 +18,13 @@
 //   next warp          tcgen05 issuer + TMEM owner.
 //   2*NVB warps        epilogue (TMEM quadrants 2-3): o rows, scaled, bf16.
 // Every MMA uses M = 128 (one TMEM lane per accumulator row):
-//   ACC[buf] = [w ; qg] @ h           lanes 0-63 = WH, lanes 64-127 = qg@h
-//   DH       = kg^T @ v'              (kg read MN-major; 128 lanes = K rows)
-//   ACC[buf] += [unused ; Aqk] @ v'   lanes 64-127 become qg@h + Aqk@v'
+//   ACC[buf]  = [I ; 0] @ u            lanes 0-63 = u (exact), 64-127 = 0
+//   ACC[buf] += -[w ; qg] @ h          lanes 0-63 = u - WH = v', 64-127 = -qg@h
+//   DH        = kg^T @ v'              (kg read MN-major; 128 lanes = K rows)
+//   ACC[buf] += -[unused ; Aqk] @ v'   lanes 64-127 = -(qg@h + Aqk@v')
+// (the A operand negated through the instruction descriptor; the epilogue
+// scales by -scale).  The u term needs no state, so it is issued ahead, while
+// the previous chunk's state update runs, and v' leaves TMEM ready to round.
 // The critical path WH -> v' -> DH -> h -> next WH is issued first; the output
 // MMA and the epilogue overlap it, ACC is double-buffered across chunks, and
 // the input ring lets the loads of the next chunks overlap the current one.
@@ -78,7 +82,9 @@ struct ScanCfg {
     static constexpr uint32_t HS = STAGES * STAGE;       // h bf16 per V block [K rows][64 v], MN-major SW128
     static constexpr uint32_t HS_BLOCK = KB * 8192;
     static constexpr uint32_t VP = HS + NVB * HS_BLOCK;  // v' bf16 per V block [64 tok][64 v], MN-major SW128
-    static constexpr uint32_t BYTES = VP + NVB * 8192;
+    // [I_64 ; 0] bf16, K-major SW128 [128 rows][64 tok]: the A operand that puts u into the accumulator
+    static constexpr uint32_t IDN = VP + NVB * 8192;
+    static constexpr uint32_t BYTES = IDN + 16384;
 };
 
 template <int STAGES>
@@ -156,6 +162,28 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         tmem_alloc(&B.tmem_slot, S::TMEM_COLS);
         tmem_relinquish();
     }
+    // [I ; 0] operand; in map mode the u slots of P column blocks are never
+    // loaded and hold zeros (those columns see u = 0)
+    for (int e = tid; e < 16384 / 16; e += S::THREADS) {
+        const int row = e >> 3, ch = e & 7;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        // row < 64: 1.0 at column row, i.e. in 16-byte chunk (row / 8) ^ (row & 7)
+        if (row < 64 && ch == ((row >> 3) ^ (row & 7))) {
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            wv[(row & 7) >> 1] = (row & 1) ? 0x3F800000u : 0x00003F80u;
+            x = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        *reinterpret_cast<uint4*>(sm + S::IDN + e * 16) = x;
+    }
+    if (map_mode) {
+        for (int vb = 0; vb < NVB; ++vb) {
+            if (v0 + vb * 64 >= K) continue;
+            for (int e = tid; e < STAGES * 512; e += S::THREADS)
+                *reinterpret_cast<uint4*>(sm + (e >> 9) * S::STAGE + S::U + vb * 8192 + (e & 511) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -246,27 +274,22 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             if (!wait(&B.full[st], sp)) break;
             if (quad < 2) {
                 // v'[r, :] = u[r, :] - WH[r, :]
+                // v'[r, :] = u[r, :] - WH[r, :], formed in TMEM by the MMAs
                 if (!wait(&B.wh_full, it & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16) {
-                    float wh[16];
+                    float x[16];
                     tmem_ld16(t_acc + (uint32_t)((it & 1) * S::BV + vb * 64) + ((uint32_t)(quad * 32) << 16) + c0,
-                              wh);
+                              x);
                     tmem_ld_wait();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = (c0 >> 3) + hh;
-                        const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
-                        const uint4 uv = p_block ? make_uint4(0u, 0u, 0u, 0u)
-                                                 : *reinterpret_cast<const uint4*>(stage + S::U + vb * 8192 + off);
-                        const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-                        uint32_t pw[4];
-#pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            pw[t] = pack_bf16x2(bf_lo(uw[t]) - wh[8 * hh + 2 * t],
-                                                bf_hi(uw[t]) - wh[8 * hh + 2 * t + 1]);
-                        *reinterpret_cast<uint4*>(vp + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        const float* y = x + 8 * hh;
+                        *reinterpret_cast<uint4*>(vp + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                       pack_bf16x2(y[6], y[7]));
                     }
                 }
                 fence_proxy_async_smem();
@@ -358,7 +381,8 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
     } else if (warp == S::MMA_WARP) {
         // ================= tcgen05 issuer =================
         if (lane == 0) {
-            constexpr uint32_t id_h = idesc_bf16_f32(128, S::BV, 0, 1);   // A K-major, B (h, v') MN-major
+            constexpr uint32_t id_h = idesc_bf16_f32(128, S::BV, 0, 1);   // A K-major, B (u, h, v') MN-major
+            constexpr uint32_t id_hn = idesc_bf16_f32(128, S::BV, 0, 1, 1);  // the same with A negated
             constexpr uint32_t id_dh = idesc_bf16_f32(128, S::BV, 1, 1);  // A = kg^T MN-major
             for (int it = 0; it < nit && !*abort_flag; ++it) {
                 const int st = it % STAGES;
@@ -367,15 +391,21 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 const uint32_t bp = (it >> 1) & 1;
                 const uint32_t stage = sbase + st * S::STAGE;
                 if (!wait(&B.full[st], sp)) break;
-                if (!wait(&B.h_ready, it & 1)) break;
                 if (!wait(&B.acc_empty[buf], bp ^ 1)) break;
                 tc_fence_after();
                 const uint32_t d_acc = t_acc + buf * S::BV;
+                // ACC = [I ; 0] @ u, ahead of the state
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(d_acc, smem_desc(sbase + S::IDN + ks * 32, 16, 1024),
+                             smem_desc(stage + S::U + ks * 2048, 8192, 1024), id_h, ks > 0 ? 1u : 0u);
+                if (!wait(&B.h_ready, it & 1)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks) {
                     const int kb = ks >> 2, kk = ks & 3;
                     mma_bf16(d_acc, smem_desc(stage + S::AW + kb * 16384 + kk * 32, 16, 1024),
-                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_h, ks > 0 ? 1u : 0u);
+                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_hn, 1u);
                 }
                 mma_commit(&B.wh_full);
                 if (!wait(&B.vp_ready, it & 1)) break;
@@ -389,7 +419,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16(d_acc, smem_desc(stage + S::AQK - 8192 + ks * 32, 16, 1024),
-                                 smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_h, 1u);
+                                 smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_hn, 1u);
                 }
                 mma_commit(&B.acc_full[buf]);
                 mma_commit(&B.empty[st]);
@@ -424,23 +454,24 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.acc_empty[buf]);
                 const int valid = min(64, si.len - c * 64);
+                const float nscale = -scale;  // the accumulator holds -(qg@h + Aqk@v')
                 if (i < valid) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         o + ((int64_t)(si.bos + c * 64 + i) * H + h) * V + v0 + vb * 64);
                     if (flags & kScanOutF16) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            dst[j] = make_uint4(pack_f16x2(scale * acc[8 * j], scale * acc[8 * j + 1]),
-                                                pack_f16x2(scale * acc[8 * j + 2], scale * acc[8 * j + 3]),
-                                                pack_f16x2(scale * acc[8 * j + 4], scale * acc[8 * j + 5]),
-                                                pack_f16x2(scale * acc[8 * j + 6], scale * acc[8 * j + 7]));
+                            dst[j] = make_uint4(pack_f16x2(nscale * acc[8 * j], nscale * acc[8 * j + 1]),
+                                                pack_f16x2(nscale * acc[8 * j + 2], nscale * acc[8 * j + 3]),
+                                                pack_f16x2(nscale * acc[8 * j + 4], nscale * acc[8 * j + 5]),
+                                                pack_f16x2(nscale * acc[8 * j + 6], nscale * acc[8 * j + 7]));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            dst[j] = make_uint4(pack_bf16x2(scale * acc[8 * j], scale * acc[8 * j + 1]),
-                                                pack_bf16x2(scale * acc[8 * j + 2], scale * acc[8 * j + 3]),
-                                                pack_bf16x2(scale * acc[8 * j + 4], scale * acc[8 * j + 5]),
-                                                pack_bf16x2(scale * acc[8 * j + 6], scale * acc[8 * j + 7]));
+                            dst[j] = make_uint4(pack_bf16x2(nscale * acc[8 * j], nscale * acc[8 * j + 1]),
+                                                pack_bf16x2(nscale * acc[8 * j + 2], nscale * acc[8 * j + 3]),
+                                                pack_bf16x2(nscale * acc[8 * j + 4], nscale * acc[8 * j + 5]),
+                                                pack_bf16x2(nscale * acc[8 * j + 6], nscale * acc[8 * j + 7]));
                     }
                 }
             }
