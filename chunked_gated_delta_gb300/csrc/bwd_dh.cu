@@ -24,10 +24,13 @@
 //                      tile as bf16 for the qg^T @ do product.
 //   next warp          tcgen05 issuer + TMEM owner.
 // MMAs, all M = 128:
-//   DV = [kg ; qg] @ dh      TMEM lanes 0-63 (rows 64-127 unused)
-//   QD = qg^T @ do           qg read MN-major; 128 lanes = K rows
-//   WD = w^T @ dv2           w read MN-major
-// The chain DV -> dv2 -> WD -> dh -> next DV is issued first; QD overlaps it.
+//   DV  = [I ; *] @ dv_in     TMEM lanes 0-63 = dv_in exactly (lanes 64-127 unused)
+//   DV += [kg ; qg] @ dh      lanes 0-63 = dv2 before rounding
+//   QD  = qg^T @ do           qg read MN-major; 128 lanes = K rows; two buffers
+//   WD  = w^T @ dv2           w read MN-major
+// DV's dv_in term and QD need no state: they are issued as soon as a chunk's
+// tiles land, during the previous chunk's update, so the chain
+// DV -> dv2 -> WD -> dh -> next DV carries only the state-dependent products.
 // Rows of a tail chunk past the sequence end have qg = kg = w = 0 in the
 // workspace, so do there contributes nothing; dv2 rows there are masked.
 //
@@ -88,7 +91,11 @@ struct BwdCfg {
     // persistent
     static constexpr uint32_t HS = STAGES * STAGE;         // dh bf16 per V block [K rows][64 v], MN-major
     static constexpr uint32_t HS_BLOCK = KB * 8192;
-    static constexpr uint32_t VP = HS + NVB * HS_BLOCK;    // dv2 bf16 per V block [64 tok][64 v], MN-major
+    // I_64 (bf16, or fp16 with fp16 gradients), K-major SW128 [64 rows][64 tok]:
+    // the A operand that puts dv_in into the accumulator; its rows 64-127 read
+    // the next 8 KB (VP), which land in unused TMEM lanes
+    static constexpr uint32_t IDN = HS + NVB * HS_BLOCK;
+    static constexpr uint32_t VP = IDN + 8192;             // dv2 bf16 per V block [64 tok][64 v], MN-major
     static constexpr uint32_t BYTES = VP + NVB * 8192;
 };
 
@@ -160,6 +167,19 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         tmem_alloc(&B.tmem_slot, S::TMEM_COLS);
         tmem_relinquish();
     }
+    for (int e = tid; e < 8192 / 16; e += S::THREADS) {
+        const int row = e >> 3, ch = e & 7;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        // 1.0 at column row, i.e. in 16-byte chunk (row / 8) ^ (row & 7)
+        if (ch == ((row >> 3) ^ (row & 7))) {
+            const uint32_t one = F16 ? 0x3C00u : 0x3F80u;
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            wv[(row & 7) >> 1] = (row & 1) ? one << 16 : one;
+            x = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        *reinterpret_cast<uint4*>(sm + S::IDN + e * 16) = x;
+    }
+    fence_proxy_async_smem();
     if (map_mode) {
         // P columns see do = dv_in = 0: their tiles stay zero in every stage
         // (the TMA never writes them)
@@ -177,7 +197,8 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B.tmem_slot;
-    const uint32_t t_dv = tmem, t_qd = tmem + S::BV, t_wd = tmem + 2 * S::BV;
+    // TMEM columns: DV, WD, then QD for even and odd chunks
+    const uint32_t t_dv = tmem, t_wd = tmem + S::BV, t_qd = tmem + 2 * S::BV;
     volatile int* abort_flag = &B.abort_flag;
     bool timed_out = false;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -269,33 +290,22 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 uint4* gdst = reinterpret_cast<uint4*>(dv2 + ((int64_t)(si.bos + c * 64 + r) * H + h) * V + col);
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16) {
-                    float dv[16];
+                    float dv[16];  // kg@dh + dv_in, summed by the MMAs
                     tmem_ld16(t_dv + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, dv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = (c0 >> 3) + hh;
                         const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
-                        const uint4 iv = *reinterpret_cast<const uint4*>(stage + S::DVIN + vb * 8192 + off);
-                        const uint32_t iw[4] = {iv.x, iv.y, iv.z, iv.w};
+                        const float* x = dv + 8 * hh;
                         uint32_t pw[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) pw[t] = row_ok ? pack_bf16x2(x[2 * t], x[2 * t + 1]) : 0u;
                         if constexpr (F16) {
-                            uint32_t ph[4];
-#pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const float x0 = dv[8 * hh + 2 * t] + h_lo(iw[t]);
-                                const float x1 = dv[8 * hh + 2 * t + 1] + h_hi(iw[t]);
-                                pw[t] = row_ok ? pack_bf16x2(x0, x1) : 0u;
-                                ph[t] = pack_f16x2(x0, x1);
-                            }
                             // fp16 dv2 leaves from the fp32 values (the operand copy is bf16)
-                            if (row_ok && !map_mode) gdst[cc] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                        } else {
-#pragma unroll
-                            for (int t = 0; t < 4; ++t)
-                                pw[t] = row_ok ? pack_bf16x2(dv[8 * hh + 2 * t] + bf_lo(iw[t]),
-                                                             dv[8 * hh + 2 * t + 1] + bf_hi(iw[t]))
-                                               : 0u;
+                            if (row_ok && !map_mode)
+                                gdst[cc] = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]),
+                                                      pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
                         }
                         *reinterpret_cast<uint4*>(vp + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                     }
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 8) {
                     float qd[8], wd[8];
-                    tmem_ld8(t_qd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, qd);
+                    tmem_ld8(t_qd + (uint32_t)((it & 1) * S::BV + vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, qd);
                     tmem_ld8(t_wd + (uint32_t)(vb * 64) + ((uint32_t)(quad * 32) << 16) + c0, wd);
                     tmem_ld_wait();
 #pragma unroll
@@ -420,27 +430,39 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         if (lane == 0) {
             constexpr uint32_t id_dv = idesc_bf16_f32(128, S::BV, 0, 1);  // A K-major, B (dh) MN-major
             constexpr uint32_t id_up = idesc_bf16_f32(128, S::BV, 1, 1);  // A (qg^T, w^T) MN-major
+            // the dv_in term: fp16 operands with fp16 gradients
+            constexpr uint32_t id_in = F16 ? idesc_f16_f32(128, S::BV, 0, 1) : idesc_bf16_f32(128, S::BV, 0, 1);
             for (int it = 0; it < nit && !*abort_flag; ++it) {
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
                 const uint32_t stage = sbase + st * S::STAGE;
                 if (!wait(&B.full[st], sp)) break;
+                tc_fence_after();
+                // DV = dv_in (the previous chunk's dv2 phase has read DV: its
+                // vp_ready was waited on before this point)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(t_dv, smem_desc(sbase + S::IDN + ks * 32, 16, 1024),
+                             smem_desc(stage + S::DVIN + ks * 2048, 8192, 1024), id_in, ks > 0 ? 1u : 0u);
+                // QD = qg^T @ do into this chunk's buffer (the update two chunks
+                // back, which read it, finished before the last h_ready): the
+                // qg blocks sit 16 KB apart (K = 64: the next 8 KB are unused rows)
+                if (f16 && !wait(&B.do_ready[st], sp)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(t_qd + (uint32_t)((it & 1) * S::BV),
+                             smem_desc(stage + S::AKQ + 8192 + ks * 2048, KB == 2 ? 16384 : 8192, 1024),
+                             smem_desc(stage + S::DO + ks * 2048, 8192, 1024), id_up, ks > 0 ? 1u : 0u);
                 if (!wait(&B.h_ready, it & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks) {
                     const int kb = ks >> 2, kk = ks & 3;
                     mma_bf16(t_dv, smem_desc(stage + S::AKQ + kb * 16384 + kk * 32, 16, 1024),
-                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_dv, ks > 0 ? 1u : 0u);
+                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_dv, 1u);
                 }
                 mma_commit(&B.dv_full);
-                // QD = qg^T @ do: the qg blocks sit 16 KB apart (K = 64: the next 8 KB are unused rows)
-                if (f16 && !wait(&B.do_ready[st], sp)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(t_qd, smem_desc(stage + S::AKQ + 8192 + ks * 2048, KB == 2 ? 16384 : 8192, 1024),
-                             smem_desc(stage + S::DO + ks * 2048, 8192, 1024), id_up, ks > 0 ? 1u : 0u);
                 if (!wait(&B.vp_ready, it & 1)) break;
                 tc_fence_after();
 #pragma unroll

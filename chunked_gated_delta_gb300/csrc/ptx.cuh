@@ -233,6 +233,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
+// The same with fp16 A/B (one MMA never mixes fp16 and bf16 operands).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+    return idesc_bf16_f32(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10));  // A, B format: f16 (0)
+}
+
 // Byte offset of element (row, col) of a bf16 tile stored as 128-byte swizzled
 // rows of 64 elements (one SW128 column block; row = 128 bytes).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
