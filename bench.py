@@ -64,9 +64,17 @@ def flops_per_token_head(K, V, C=64):
     return per_chunk / C
 
 
+# headers every kernel translation unit compiles in (PTX wrappers, layouts)
+KERNEL_HEADERS = ("ptx.cuh", "common.cuh", "internal.h")
+
+
 def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a kernel source together with the headers it includes."""
+    h = hashlib.sha256()
+    for p in [path] + [os.path.join(os.path.dirname(path), n) for n in KERNEL_HEADERS]:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_name, src_file, workload):
