@@ -520,10 +520,7 @@ cudaError_t launch_bwd_k(const BwdArgs& a, int mode, cudaStream_t stream, int sm
 }  // namespace
 
 cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 148;
+    const int sms = device_sm_count();
     if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
     auto run = [&](int mode) {
         return a.K == 128 ? launch_bwd_k<2>(a, mode, stream, sms) : launch_bwd_k<1>(a, mode, stream, sms);

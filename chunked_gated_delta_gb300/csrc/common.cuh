@@ -74,6 +74,15 @@ inline ScanShape scan_shape(int64_t ctas64, int ncol, int sms) {
 // 10%; segments are never shorter than kSegMinChunks.  It depends on the dims
 // only (so does the workspace size).
 constexpr int kPlanSMs = 148;
+
+// SMs of the current device (kPlanSMs if the query fails).
+inline int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = kPlanSMs;
+    return sms;
+}
 constexpr int kSegMinChunks = 16;
 constexpr int kSegMaxCount = 64;
 

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                      const __grid_constant__ CUtensorMap st_w, const __grid_constant__ CUtensorMap st_u,
                      const float* __restrict__ g, const uint16_t* __restrict__ beta, uint8_t* __restrict__ ws,
                      const WsLayout L, const int H, const int flags, const int group, const int beta_stride,
-                     const int beta_head0) {
+                     const int beta_head0, const int pf_dist) {
     using S = IntraSmem<KB, VB>;
     constexpr int K = S::K, V = S::V, NCG = S::NCG, NSEG = S::NSEG, RS = S::RS;
     extern __shared__ uint8_t smem_raw[];
@@ -230,6 +230,27 @@ __global__ void __launch_bounds__(kThreads, 4)
             gv[r][1] = x.y;
             gv[r][2] = x.z;
             gv[r][3] = x.w;
+        }
+    }
+    // L2 prefetch of the inputs of the tile pf_dist ahead in launch order: the
+    // tile a CTA starting about half a CTA lifetime from now takes, so its
+    // loads find q, k, v and g in L2 instead of waiting on DRAM
+    if (warp == 1 && pf_dist > 0 && tile + pf_dist < (int64_t)gridDim.x) {
+        const int64_t pt = tile + pf_dist;
+        const int pc = static_cast<int>(pt / H), ph = static_cast<int>(pt % H);
+        const ChunkInfo pci = reinterpret_cast<const ChunkInfo*>(ws + L.chunk_info)[pc];
+        if (pci.valid > 0) {
+            if (lane == 0) {
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_prefetch_3d(&tm_q, kb * 64, ph / group, pci.row0);
+                    tma_prefetch_3d(&tm_k, kb * 64, ph / group, pci.row0);
+                }
+#pragma unroll
+                for (int vb = 0; vb < VB; ++vb) tma_prefetch_3d(&tm_v, vb * 64, ph, pci.row0);
+            }
+            for (int i = lane; i < pci.valid; i += 32)
+                bulk_prefetch_l2(g + ((int64_t)(pci.row0 + i) * H + ph) * K, K * 4);
         }
     }
     if (tid == 0) {
@@ -683,9 +704,14 @@ cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t ctas = a.max_chunks * a.H;
     if (ctas <= 0) return cudaSuccess;
+    // prefetch distance in tiles, measured at 4 tiles resident per SM: 1.25 x
+    // SMs (about a third of a tile lifetime ahead) ran best at K = 128 (0.460
+    // -> 0.434 ms at the headline; half an SM-count or less, and 4 x SMs, ran
+    // slower than none); at K = 64 every distance tried ran slower, so off
+    const int pf_dist = KB == 2 ? 5 * device_sm_count() / 4 : 0;
     kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.st_qg, a.st_w, a.st_u, a.g,
                                                      a.beta, a.ws, a.L, a.H, a.flags, a.group, a.beta_stride,
-                                                     a.beta_head0);
+                                                     a.beta_head0, pf_dist);
     return cudaGetLastError();
 }
 

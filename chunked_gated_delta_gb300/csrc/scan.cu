@@ -658,10 +658,7 @@ cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, i
 }
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 148;
+    const int sms = device_sm_count();
     if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
     auto run = [&](int mode) {
         return a.K == 128 ? launch_scan_k<2>(a, mode, stream, sms) : launch_scan_k<1>(a, mode, stream, sms);
