@@ -160,3 +160,42 @@ def make_variant_inputs(w: Workload, io_dtype=torch.bfloat16, qk_heads=None, bet
     h0 = (0.1 * torch.randn((N, H, K, V), generator=gen, dtype=torch.float32)).to(state_dtype) if w.h0 else None
     return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=K ** -0.5,
                 B=B, T=T, H=H, K=K, V=V, N=N, qk_heads=Hqk, beta_logits=beta_logits)
+
+
+def make_inputs_on(w: Workload, device, with_bwd: bool = False):
+    """Inputs of the fixed-length workload ``w`` drawn directly on ``device``
+    with a generator seeded there (the distributions of :func:`make_inputs`).
+
+    For problems whose tensors are too large to draw on the CPU in a test's
+    time: the bits differ from :func:`make_inputs` (another generator), so a
+    caller hands the oracle the slices it checks, copied back from the
+    device.  ``with_bwd`` adds do, dv_in (N(0,1) bf16) and dht (N(0, 0.1^2)
+    fp32), as :func:`make_bwd_inputs` draws them.
+    """
+    if w.varlen:
+        raise ValueError("make_inputs_on draws fixed-length workloads only")
+    gen = torch.Generator(device=device).manual_seed(w.seed)
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+
+    def randn(shape):
+        return torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+
+    def unit_rows(shape):
+        x = randn(shape)
+        x /= x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        return x.to(torch.bfloat16)
+
+    q = unit_rows((B, T, H, K))
+    k = unit_rows((B, T, H, K))
+    v = randn((B, T, H, V)).to(torch.bfloat16)
+    beta = torch.sigmoid(randn((B, T, H))).to(torch.bfloat16)
+    g = randn((B, T, H, K))
+    g += w.mu
+    g = F.logsigmoid(g)
+    h0 = 0.1 * randn((B, H, K, V)) if w.h0 else None
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=None, scale=K ** -0.5,
+               B=B, T=T, H=H, K=K, V=V, N=B)
+    if with_bwd:
+        out.update(do=randn((B, T, H, V)).to(torch.bfloat16), dv_in=randn((B, T, H, V)).to(torch.bfloat16),
+                   dht=0.1 * randn((B, H, K, V)))
+    return out
