@@ -231,6 +231,13 @@ def workload_config(w, x):
             "parallelism": "independent replica per GPU"}
 
 
+def launches_per_step(lay):
+    """Kernel launches of one kda_fwd call for a workspace layout."""
+    if lay.stage_count > 1:
+        return 1 + 2 * lay.stage_count
+    return 3 + (2 if lay.seg_count > 1 else 0)
+
+
 def run_gb300(args):
     import torch
     rank, world, local = rank_info()
@@ -309,6 +316,7 @@ def run_gb300(args):
     tokens = B * T
     value = tokens * world / (ms_per_step / 1e3)
 
+    lay = kda.workspace_layout(dims)
     # roofline of the dominant kernel
     hbm, tc, tc_sus, peak_kind = peaks()
     b_intra, b_scan = bytes_per_token_head(K, V)
@@ -341,10 +349,13 @@ def run_gb300(args):
                           "flops": step_flops, "tc_ms": step_flops / (tc * 1e12) * 1e3,
                           "frac_of_hbm_bound": (step_bytes / (hbm * 1e9) * 1e3) / ms_per_step},
         "kernels_ms": {"intra": intra_avg, "scan": scan_avg, "note": "separate split steps with an event "
-                       "between the kernels; the timed steps run them back to back"},
+                       "between the kernels over every chunk; the timed steps run them back to back"
+                       + (f", in {lay.stage_count} chunk ranges of {lay.stage_len} chunks (each range's "
+                          "intra kernel beside the previous range's scan)" if lay.stage_count > 1 else "")},
         "e2e": e2e,
-        # planner + intra + scan (+ map pass and combine when the scan is segmented)
-        "gpu_launches": (3 + (2 if kda.workspace_layout(dims).seg_count > 1 else 0)) * args.steps,
+        # planner + intra + scan (+ map pass and combine when the scan is segmented;
+        # planner + one intra and one scan per chunk range when the forward is staged)
+        "gpu_launches": launches_per_step(lay) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

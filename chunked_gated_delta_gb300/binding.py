@@ -55,7 +55,8 @@ class WsLayout(ctypes.Structure):
                 ("status", "seq_info", "chunk_info", "gd", "qg", "kg", "w", "u", "aqk", "total")] + [
         ("max_chunks", ctypes.c_int32), ("chunk", ctypes.c_int32),
         ("seg_count", ctypes.c_int32), ("seg_len", ctypes.c_int32),
-        ("pq", ctypes.c_size_t), ("hin", ctypes.c_size_t)]
+        ("pq", ctypes.c_size_t), ("hin", ctypes.c_size_t),
+        ("stage_count", ctypes.c_int32), ("stage_len", ctypes.c_int32)]
 
 
 def library_path() -> str:

@@ -43,8 +43,10 @@ inline int64_t max_chunks(const kda_dims& d, bool varlen) {
 struct WsLayout {
     size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, pq, hin, total;
     int64_t max_chunks;
-    int32_t seg_count;  // segments per sequence of the segmented scan (1 = plain scan)
-    int32_t seg_len;    // chunks per segment
+    int32_t seg_count;    // segments per sequence of the segmented scan (1 = plain scan)
+    int32_t seg_len;      // chunks per segment
+    int32_t stage_count;  // chunk ranges of the staged forward (1 = not staged)
+    int32_t stage_len;    // chunks per range
 };
 
 // Scan kernel shape for a launch of ctas64 64-column blocks over ncol
@@ -118,6 +120,32 @@ inline void seg_plan(const kda_dims& d, bool varlen, int32_t* count, int32_t* le
     *len = (int32_t)(best_S > 1 ? best_L : 0x7fffffff);
 }
 
+// Staged forward.  One sequence whose scan occupies at most half of the SMs
+// (and that the segmented plan leaves unsegmented, e.g. 32 heads x 65536
+// tokens at K = V = 128: 64 scan CTAs) is run as stage_count chunk ranges: the
+// intra-chunk kernel of range j + 1 runs on the idle SMs while the scan walks
+// range j, and the scan hands its fp32 state from range to range through the
+// hin region.  Ranges are at least kStageMinChunks chunks long; at most
+// kStageMax of them.  A function of the dims only (so is the workspace size).
+constexpr int kStageMinChunks = 64;
+constexpr int kStageMax = 8;
+
+inline void stage_plan(const kda_dims& d, bool varlen, int32_t seg_count, int32_t* count, int32_t* len) {
+    *count = 1;
+    *len = 0x7fffffff;
+    const int64_t N = varlen ? d.num_seqs : d.B;
+    if (N != 1 || seg_count > 1) return;
+    const int64_t ctas64 = (int64_t)d.H * (d.V / 64);  // the plain scan's 64-column blocks
+    if (2 * ctas64 > kPlanSMs) return;
+    const int64_t nt = ((int64_t)d.T + kChunk - 1) / kChunk;
+    int64_t P = nt / kStageMinChunks;
+    if (P > kStageMax) P = kStageMax;
+    if (P < 2) return;
+    const int64_t len_c = (nt + P - 1) / P;
+    *count = (int32_t)((nt + len_c - 1) / len_c);
+    *len = (int32_t)len_c;
+}
+
 inline WsLayout ws_layout(const kda_dims& d, bool varlen) {
     WsLayout L{};
     const int64_t N = varlen ? d.num_seqs : d.B;
@@ -143,11 +171,13 @@ inline WsLayout ws_layout(const kda_dims& d, bool varlen) {
     L.aqk = off;
     off = align_up(off + tiles * kChunk * kChunk * 2, 1024);
     seg_plan(d, varlen, &L.seg_count, &L.seg_len);
+    stage_plan(d, varlen, L.seg_count, &L.stage_count, &L.stage_len);
     const size_t seg_units = L.seg_count > 1 ? (size_t)L.seg_count * N * d.H : 0;
+    const size_t stage_units = L.stage_count > 1 ? (size_t)L.stage_count * N * d.H : 0;
     L.pq = off;  // fp32 [S, N, H, K, K + V]: per segment [P | Q]
     off = align_up(off + seg_units * d.K * (d.K + d.V) * sizeof(float), 1024);
-    L.hin = off;  // fp32 [S, N, H, K, V]: state entering each segment
-    off = align_up(off + seg_units * d.K * d.V * sizeof(float), 1024);
+    L.hin = off;  // fp32 [S, N, H, K, V]: state entering each segment (or stage)
+    off = align_up(off + (seg_units > stage_units ? seg_units : stage_units) * d.K * d.V * sizeof(float), 1024);
     L.total = off;
     L.max_chunks = NC;
     return L;

@@ -30,6 +30,8 @@ constexpr int kScanOutF16 = 1;     // o is fp16 (else bf16)
 constexpr int kScanStateBF16 = 2;  // h0 / ht are bf16 (else fp32)
 constexpr int kScanModeOutput = 0;  // the scan with its output o (and ht)
 constexpr int kScanModeMap = 1;     // per-segment affine maps [P | Q] (segmented scan)
+constexpr int kScanExitToHin = 4;   // output mode: a segment that ends before its sequence
+                                    // stores its exit state as the next one's entry (hin)
 
 struct ScanArgs {
     CUtensorMap tm_w, tm_qg, tm_kg, tm_u, tm_aqk;  // workspace tiles, 2-D {dim, tiles*64}
@@ -64,6 +66,11 @@ cudaError_t launch_plan(const int32_t* cu_seqlens, int N, int B, int T, uint8_t*
                         const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_intra(const IntraArgs& a, cudaStream_t stream);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
+// The scan over chunk range `stage` of the staged forward (a.L.stage_count >
+// 1): from h0 (stage 0) or the entry state in hin, writing o for the range and
+// the exit state to hin (or ht after the last range).  The CTAs reserve shared
+// memory beyond their own need, so no intra-chunk CTA shares an SM with them.
+cudaError_t launch_scan_stage(const ScanArgs& a, int stage, cudaStream_t stream);
 cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream);
 // h_in[j+1] = P_j h_in[j] + Q_j over the segment maps in L.pq (h_in[0] = h0)
 cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, int N, int H, int K, int V,

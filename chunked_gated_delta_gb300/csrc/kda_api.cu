@@ -1,6 +1,7 @@
 // kda_api.cu -- the C ABI (include/kda.h): argument validation, workspace
 // layout, TMA descriptor creation, the chunk planner kernel, and the launches
 // of the intra-chunk and scan kernels on the caller's stream.
+#include <algorithm>
 #include <cstring>
 
 #include "../../include/kda.h"
@@ -173,6 +174,8 @@ kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out) {
     out->seg_len = L.seg_len;
     out->pq = L.pq;
     out->hin = L.hin;
+    out->stage_count = L.stage_count;
+    out->stage_len = L.stage_len;
     return KDA_OK;
 }
 
@@ -193,11 +196,15 @@ int32_t kda_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int32_t chu
 }
 
 namespace {
-// kda_fwd_intra_ex with beta read as rows of beta_stride elements starting at
-// column beta_head0 (the host pipeline passes a head group's view of beta)
-kda_status intra_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
-                      int beta_stride, int beta_head0, const int32_t* cu_seqlens, const kda_dims* dims,
-                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, void* stream) {
+// Validation and TMA descriptors of the intra-chunk stage, with beta read as
+// rows of beta_stride elements starting at column beta_head0 (the host
+// pipeline passes a head group's view of beta).  Launches nothing.  *run is
+// false when there is nothing to compute past the planner (no rows or no
+// chunks); a->ws and a->L are set either way.
+kda_status intra_setup(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                       int beta_stride, int beta_head0, const int32_t* cu_seqlens, const kda_dims* dims,
+                       const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, IntraArgs* a,
+                       bool* run) {
     if (!dims) return KDA_ERR_INVALID_ARG;
     kda_fwd_opts op{};
     if (opts) op = *opts;
@@ -216,39 +223,170 @@ kda_status intra_impl(const void* q, const void* k, const void* v, const float* 
         if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(beta, 2))
             return KDA_ERR_ALIGNMENT;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const int N = varlen ? dims->num_seqs : dims->B;
-    kda_plan_kernel<<<1, kPlanThreads, 0, s>>>(cu_seqlens, N, dims->B, dims->T, ws, L);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    if (rows == 0 || L.max_chunks == 0) return KDA_OK;
-    IntraArgs a{};
+    *a = IntraArgs{};
+    a->ws = ws;
+    a->L = L;
+    *run = rows > 0 && L.max_chunks > 0;
+    if (!*run) return KDA_OK;
     const CUtensorMapDataType io =
         op.io_dtype == KDA_IO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int hqk = op.qk_heads > 0 ? op.qk_heads : dims->H;
-    bool ok = map3(&a.tm_q, io, 2, q, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && map3(&a.tm_k, io, 2, k, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && map3(&a.tm_v, io, 2, v, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    bool ok = map3(&a->tm_q, io, 2, q, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a->tm_k, io, 2, k, dims->K, hqk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && map3(&a->tm_v, io, 2, v, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     const int64_t trows = L.max_chunks * dims->H * kChunk;
-    ok = ok && map2(&a.st_qg, ws + L.qg, dims->K, trows);
-    ok = ok && map2(&a.st_w, ws + L.w, dims->K, trows);
-    ok = ok && map2(&a.st_u, ws + L.u, dims->V, trows);
+    ok = ok && map2(&a->st_qg, ws + L.qg, dims->K, trows);
+    ok = ok && map2(&a->st_w, ws + L.w, dims->K, trows);
+    ok = ok && map2(&a->st_u, ws + L.u, dims->V, trows);
     if (!ok) return KDA_ERR_CUDA;
-    a.g = g;
-    a.beta = static_cast<const uint16_t*>(beta);
-    a.ws = ws;
-    a.L = L;
-    a.H = dims->H;
-    a.K = dims->K;
-    a.V = dims->V;
-    a.max_chunks = L.max_chunks;
-    a.f16 = op.io_dtype == KDA_IO_F16;
-    a.flags = op.beta_logits ? kIntraBetaLogits : 0;
-    a.group = dims->H / hqk;
-    a.beta_stride = beta_stride;
-    a.beta_head0 = beta_head0;
-    if (launch_intra(a, s) != cudaSuccess) return KDA_ERR_CUDA;
+    a->g = g;
+    a->beta = static_cast<const uint16_t*>(beta);
+    a->H = dims->H;
+    a->K = dims->K;
+    a->V = dims->V;
+    a->max_chunks = L.max_chunks;
+    a->f16 = op.io_dtype == KDA_IO_F16;
+    a->flags = op.beta_logits ? kIntraBetaLogits : 0;
+    a->group = dims->H / hqk;
+    a->beta_stride = beta_stride;
+    a->beta_head0 = beta_head0;
     return KDA_OK;
+}
+
+// The planner: validates cu_seqlens, builds the tables, resets the status word.
+kda_status plan(const int32_t* cu_seqlens, const kda_dims* dims, const IntraArgs& a, cudaStream_t s) {
+    const int N = is_varlen(dims) ? dims->num_seqs : dims->B;
+    kda_plan_kernel<<<1, kPlanThreads, 0, s>>>(cu_seqlens, N, dims->B, dims->T, a.ws, a.L);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status intra_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                      int beta_stride, int beta_head0, const int32_t* cu_seqlens, const kda_dims* dims,
+                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, void* stream) {
+    IntraArgs a;
+    bool run = false;
+    kda_status st = intra_setup(q, k, v, g, beta, beta_stride, beta_head0, cu_seqlens, dims, opts, workspace,
+                                workspace_bytes, &a, &run);
+    if (st != KDA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = plan(cu_seqlens, dims, a, s);
+    if (st != KDA_OK || !run) return st;
+    return launch_intra(a, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// Validation and TMA descriptors of the scan stage.  Launches nothing.
+kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
+                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, ScanArgs* a) {
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    if (!check_opts(&op, dims)) return KDA_ERR_INVALID_ARG;
+    const bool varlen = is_varlen(dims);
+    kda_status st = check_dims(dims, varlen);
+    if (st != KDA_OK) return st;
+    WsLayout L;
+    st = check_ws(dims, varlen, workspace, workspace_bytes, &L);
+    if (st != KDA_OK) return st;
+    const int64_t rows = (int64_t)dims->B * dims->T;
+    if (rows > 0 && !o) return KDA_ERR_INVALID_ARG;
+    if ((o && !aligned(o, 16)) || (h0 && !aligned(h0, 16)) || (ht && !aligned(ht, 16)))
+        return KDA_ERR_ALIGNMENT;
+    *a = ScanArgs{};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t trows = L.max_chunks * dims->H * kChunk;
+    if (trows > 0) {
+        bool ok = map2(&a->tm_w, ws + L.w, dims->K, trows);
+        ok = ok && map2(&a->tm_qg, ws + L.qg, dims->K, trows);
+        ok = ok && map2(&a->tm_kg, ws + L.kg, dims->K, trows);
+        ok = ok && map2(&a->tm_u, ws + L.u, dims->V, trows);
+        ok = ok && map2(&a->tm_aqk, ws + L.aqk, kChunk, trows);
+        if (!ok) return KDA_ERR_CUDA;
+    }
+    a->h0 = h0;
+    a->ht = ht;
+    a->o = static_cast<uint16_t*>(o);
+    a->ws = ws;
+    a->L = L;
+    a->scale = scale;
+    a->N = varlen ? dims->num_seqs : dims->B;
+    a->H = dims->H;
+    a->K = dims->K;
+    a->V = dims->V;
+    a->flags = (op.io_dtype == KDA_IO_F16 ? kScanOutF16 : 0) | (op.state_dtype == KDA_STATE_BF16 ? kScanStateBF16 : 0);
+    return KDA_OK;
+}
+
+// Streams and events of the staged forward, created once per device: the
+// intra-chunk kernels of the chunk ranges run on `intra`, the scans on `scan`
+// (the highest stream priority, so a range's scan CTAs are placed before the
+// next range's intra CTAs when both are ready).
+struct StageRes {
+    bool ready = false;
+    cudaStream_t intra = nullptr, scan = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, ev_intra[2] = {}, ev_scan[2] = {};
+};
+std::mutex g_stage_mutex;
+StageRes g_stage[64];
+
+StageRes* stage_res() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    StageRes& r = g_stage[dev];
+    if (r.ready) return &r;
+    int least = 0, greatest = 0;
+    bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess;
+    ok = ok && r.intra == nullptr && cudaStreamCreateWithFlags(&r.intra, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamCreateWithPriority(&r.scan, cudaStreamNonBlocking, greatest) == cudaSuccess;
+    cudaEvent_t* evs[] = {&r.start, &r.done, &r.ev_intra[0], &r.ev_intra[1], &r.ev_scan[0], &r.ev_scan[1]};
+    for (cudaEvent_t* e : evs) ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    r.ready = ok;
+    return ok ? &r : nullptr;
+}
+
+// The chunk ranges of the staged forward (one sequence, L.stage_count > 1).
+// Range j's intra kernel waits for range j - 2's scan (so at most one range of
+// intra work runs ahead and the scan finds its SMs free), range j's scan for
+// range j's intra kernel and, by stream order, range j - 1's scan.  Forked
+// from and joined back to the caller's stream s.
+kda_status run_stages(const IntraArgs& ia, const ScanArgs& sa, cudaStream_t s) {
+    std::unique_lock<std::mutex> lock(g_stage_mutex);
+    StageRes* R = stage_res();
+    if (!R) {  // no library streams: the same work in order on the caller's stream
+        if (launch_intra(ia, s) != cudaSuccess || launch_scan(sa, s) != cudaSuccess) return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
+    if (cudaEventRecord(R->start, s) != cudaSuccess || cudaStreamWaitEvent(R->intra, R->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(R->scan, R->start, 0) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const WsLayout& L = ia.L;
+    const int64_t H = ia.H;
+    bool ok = true;
+    for (int j = 0; j < L.stage_count && ok; ++j) {
+        // range j's intra kernel sees the workspace from chunk c0 on: the same
+        // kernel, its tile index counted from the range's first chunk
+        const int64_t c0 = (int64_t)j * L.stage_len;
+        const int64_t c1 = std::min<int64_t>(c0 + L.stage_len, L.max_chunks);
+        IntraArgs aj = ia;
+        aj.max_chunks = c1 - c0;
+        aj.L.chunk_info += (size_t)c0 * sizeof(ChunkInfo);
+        aj.L.gd += (size_t)(c0 * H) * ia.K * sizeof(float);
+        aj.L.kg += (size_t)(c0 * H) * kChunk * ia.K * 2;
+        aj.L.aqk += (size_t)(c0 * H) * kChunk * kChunk * 2;
+        const int64_t rows = aj.max_chunks * H * kChunk;
+        ok = map2(&aj.st_qg, ia.ws + L.qg + (size_t)(c0 * H) * kChunk * ia.K * 2, ia.K, rows) &&
+             map2(&aj.st_w, ia.ws + L.w + (size_t)(c0 * H) * kChunk * ia.K * 2, ia.K, rows) &&
+             map2(&aj.st_u, ia.ws + L.u + (size_t)(c0 * H) * kChunk * ia.V * 2, ia.V, rows);
+        ok = ok && (j < 2 || cudaStreamWaitEvent(R->intra, R->ev_scan[j & 1], 0) == cudaSuccess) &&
+             launch_intra(aj, R->intra) == cudaSuccess && cudaEventRecord(R->ev_intra[j & 1], R->intra) == cudaSuccess &&
+             cudaStreamWaitEvent(R->scan, R->ev_intra[j & 1], 0) == cudaSuccess &&
+             launch_scan_stage(sa, j, R->scan) == cudaSuccess &&
+             cudaEventRecord(R->ev_scan[j & 1], R->scan) == cudaSuccess;
+    }
+    // join (also after a failed launch, so the caller's stream never runs ahead of enqueued work)
+    const bool joined =
+        cudaEventRecord(R->done, R->scan) == cudaSuccess && cudaStreamWaitEvent(s, R->done, 0) == cudaSuccess;
+    return ok && joined ? KDA_OK : KDA_ERR_CUDA;
 }
 }  // namespace
 
@@ -269,43 +407,9 @@ kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const floa
 kda_status kda_fwd_scan_ex(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
                            const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes,
                            void* stream) {
-    if (!dims) return KDA_ERR_INVALID_ARG;
-    kda_fwd_opts op{};
-    if (opts) op = *opts;
-    if (!check_opts(&op, dims)) return KDA_ERR_INVALID_ARG;
-    const bool varlen = is_varlen(dims);
-    kda_status st = check_dims(dims, varlen);
+    ScanArgs a;
+    kda_status st = scan_setup(scale, h0, o, ht, dims, opts, workspace, workspace_bytes, &a);
     if (st != KDA_OK) return st;
-    WsLayout L;
-    st = check_ws(dims, varlen, workspace, workspace_bytes, &L);
-    if (st != KDA_OK) return st;
-    const int64_t rows = (int64_t)dims->B * dims->T;
-    if (rows > 0 && !o) return KDA_ERR_INVALID_ARG;
-    if ((o && !aligned(o, 16)) || (h0 && !aligned(h0, 16)) || (ht && !aligned(ht, 16)))
-        return KDA_ERR_ALIGNMENT;
-    const int N = varlen ? dims->num_seqs : dims->B;
-    ScanArgs a{};
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const int64_t trows = L.max_chunks * dims->H * kChunk;
-    if (trows > 0) {
-        bool ok = map2(&a.tm_w, ws + L.w, dims->K, trows);
-        ok = ok && map2(&a.tm_qg, ws + L.qg, dims->K, trows);
-        ok = ok && map2(&a.tm_kg, ws + L.kg, dims->K, trows);
-        ok = ok && map2(&a.tm_u, ws + L.u, dims->V, trows);
-        ok = ok && map2(&a.tm_aqk, ws + L.aqk, kChunk, trows);
-        if (!ok) return KDA_ERR_CUDA;
-    }
-    a.h0 = h0;
-    a.ht = ht;
-    a.o = static_cast<uint16_t*>(o);
-    a.ws = ws;
-    a.L = L;
-    a.scale = scale;
-    a.N = N;
-    a.H = dims->H;
-    a.K = dims->K;
-    a.V = dims->V;
-    a.flags = (op.io_dtype == KDA_IO_F16 ? kScanOutF16 : 0) | (op.state_dtype == KDA_STATE_BF16 ? kScanStateBF16 : 0);
     if (launch_scan(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
@@ -372,9 +476,21 @@ kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* 
                       float scale, const void* h0, const int32_t* cu_seqlens, void* o, void* ht,
                       const kda_dims* dims, const kda_fwd_opts* opts, void* workspace,
                       size_t workspace_bytes, void* stream) {
-    kda_status st = kda_fwd_intra_ex(q, k, v, g, beta, cu_seqlens, dims, opts, workspace, workspace_bytes, stream);
+    // every argument of both stages is checked before anything is launched
+    IntraArgs ia;
+    bool run = false;
+    kda_status st = intra_setup(q, k, v, g, beta, dims ? dims->H : 0, 0, cu_seqlens, dims, opts, workspace,
+                                workspace_bytes, &ia, &run);
     if (st != KDA_OK) return st;
-    return kda_fwd_scan_ex(scale, h0, o, ht, dims, opts, workspace, workspace_bytes, stream);
+    ScanArgs sa;
+    st = scan_setup(scale, h0, o, ht, dims, opts, workspace, workspace_bytes, &sa);
+    if (st != KDA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = plan(cu_seqlens, dims, ia, s);
+    if (st != KDA_OK) return st;
+    if (run && ia.L.stage_count > 1) return run_stages(ia, sa, s);
+    if (run && launch_intra(ia, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return launch_scan(sa, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,

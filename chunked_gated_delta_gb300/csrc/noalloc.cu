@@ -53,6 +53,10 @@ extern "C" kda_status kda_fwd_noalloc(const void* q, const void* k, const void* 
     kda_status err = KDA_OK;
     void* scratch = scratch_on_current_device(&err);
     if (!scratch) return err;
-    return kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, dims, scratch, kScratchBytes,
-                   stream);
+    // the two stages in order on the caller's stream (kda_fwd may instead run a
+    // long single sequence in chunk ranges on two streams that the library
+    // creates; this entry point creates nothing)
+    kda_status st = kda_fwd_intra(q, k, v, g, beta, cu_seqlens, dims, scratch, kScratchBytes, stream);
+    if (st != KDA_OK) return st;
+    return kda_fwd_scan(scale, h0, o, ht, dims, scratch, kScratchBytes, stream);
 }

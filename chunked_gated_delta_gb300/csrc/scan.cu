@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                     const __grid_constant__ CUtensorMap tm_aqk, const void* __restrict__ h0,
                     void* __restrict__ ht, uint16_t* __restrict__ o, uint8_t* __restrict__ ws,
                     const WsLayout L, const float scale, const int N, const int H, const int V, const int flags,
-                    const int mode) {
+                    const int mode, const int seg_base) {
     using S = ScanCfg<KB, NVB, STAGES>;
     constexpr int K = S::K;
     extern __shared__ uint8_t smem_raw[];
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
     const int vt = blockIdx.x % NT;
     const int h = (blockIdx.x / NT) % H;
     const int s = blockIdx.x / (NT * H);
-    const int seg = blockIdx.y;
+    const int seg = seg_base + (int)blockIdx.y;
     const int v0 = vt * S::BV;
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
@@ -321,6 +321,14 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
+        } else if (!map_mode && c_end < tiles && (flags & kScanExitToHin) && has_row && !timed_out &&
+                   !*abort_flag) {
+            // a chunk range of the staged forward: the exit state enters the next range
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(ws + L.hin) +
+                                                    ((((int64_t)(seg + 1) * N + s) * H + h) * K + r) * V + col);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
         } else if (!map_mode && c_end == tiles && ht != nullptr && has_row && !timed_out && !*abort_flag) {
             if (flags & kScanStateBF16) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ht) + hrow);
@@ -487,35 +495,51 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
     if (timed_out) atomicOr(status, kStatusTimeout);
 }
 
+// Shared memory a scan CTA of the staged forward reserves: with it no
+// intra-chunk CTA (about 55 KB including the per-CTA reservation) fits on the
+// same SM, so the intra kernel of the next chunk range runs on the SMs the
+// scan leaves idle and does not take issue slots from the scan's serial chain.
+constexpr uint32_t kStageScanSmem = 180 * 1024;
+
+// stage < 0: the plain or segmented scan (mode); stage >= 0: chunk range
+// `stage` of the staged forward, one CTA per (sequence, head, V tile).
 template <int KB, int NVB, int STAGES>
-cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream) {
+cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream, int stage = -1) {
     using S = ScanCfg<KB, NVB, STAGES>;
-    const uint32_t smem = S::BYTES + 1024;
+    uint32_t smem = S::BYTES + 1024;
+    if (stage >= 0 && smem < kStageScanSmem) smem = kStageScanSmem;
     auto kern = kda_scan_kernel<KB, NVB, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
     const int64_t ctas = (int64_t)a.N * a.H * (ncol / S::BV);
-    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const int segs = stage >= 0 ? 1 : mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
     if (ctas <= 0 || segs <= 0) return cudaSuccess;
+    WsLayout L = a.L;
+    int flags = a.flags;
+    if (stage >= 0) {  // the kernel's segment arithmetic over the chunk ranges
+        L.seg_count = L.stage_count;
+        L.seg_len = L.stage_len;
+        flags |= kScanExitToHin;
+    }
     const dim3 grid((unsigned)ctas, (unsigned)segs);
     kern<<<grid, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.h0, a.ht, a.o, a.ws,
-                                             a.L, a.scale, a.N, a.H, a.V, a.flags, mode);
+                                             L, a.scale, a.N, a.H, a.V, flags, mode, stage >= 0 ? stage : 0);
     return cudaGetLastError();
 }
 
 template <int KB>
-cudaError_t launch_scan_k(const ScanArgs& a, int mode, cudaStream_t stream, int sms) {
+cudaError_t launch_scan_k(const ScanArgs& a, int mode, cudaStream_t stream, int sms, int stage = -1) {
     const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
-    const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const int segs = stage >= 0 ? 1 : mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
     const ScanShape sh = scan_shape((int64_t)a.N * a.H * (ncol / 64) * segs, ncol, sms);
     // Few CTAs: each SM holds at most one, so give it a two-deep input ring.
-    if (sh.nvb == 1 && sh.stages == 2) return launch_scan_t<KB, 1, 2>(a, mode, stream);
+    if (sh.nvb == 1 && sh.stages == 2) return launch_scan_t<KB, 1, 2>(a, mode, stream, stage);
     // Many CTAs with 128-column tiles: one CTA covers 128 columns, two-deep
     // ring, w/qg/kg/Aqk loaded once per 128 columns.
-    if (sh.nvb == 2) return launch_scan_t<KB, 2, 2>(a, mode, stream);
+    if (sh.nvb == 2) return launch_scan_t<KB, 2, 2>(a, mode, stream, stage);
     // Many CTAs otherwise: two CTAs per SM, one stage each.
-    return launch_scan_t<KB, 1, 1>(a, mode, stream);
+    return launch_scan_t<KB, 1, 1>(a, mode, stream, stage);
 }
 
 // Chains the segment maps of the map pass: for every (sequence, head, 16
@@ -672,6 +696,15 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     return run(kScanModeOutput);
+}
+
+cudaError_t launch_scan_stage(const ScanArgs& a, int stage, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
+    if (a.L.stage_count < 2 || a.L.seg_count > 1 || stage < 0 || stage >= a.L.stage_count)
+        return cudaErrorInvalidValue;
+    return a.K == 128 ? launch_scan_k<2>(a, kScanModeOutput, stream, sms, stage)
+                      : launch_scan_k<1>(a, kScanModeOutput, stream, sms, stage);
 }
 
 }  // namespace kda

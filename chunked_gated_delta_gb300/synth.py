@@ -52,9 +52,10 @@ WORKLOADS = {
     "varlen": Workload("varlen", B=1, T=0, H=32, K=128, V=128, varlen=16, seed=20261205),
     "long": Workload("long", B=1, T=65536, H=32, K=128, V=128, mu=5.0, h0=False,
                      seed=20261206),
-    # a quarter of the headline batch: the size profiler captures run on (its
-    # inputs, ~0.4 GB, still exceed L2)
-    "quarter": Workload("quarter", B=1, T=8192, H=32, K=128, V=128, seed=20261207),
+    # a quarter of the headline's token-heads in two sequences (so the forward
+    # runs unstaged, as at the headline): the size profiler captures of the
+    # intra kernel run on (its inputs, ~0.4 GB, still exceed L2)
+    "quarter": Workload("quarter", B=2, T=4096, H=32, K=128, V=128, seed=20261207),
     # the same token-heads as "quarter" spread over 128 heads: the scan kernel
     # runs the headline's grid (128 CTAs, 128-wide V tiles) on 32 chunks each
     "wide": Workload("wide", B=1, T=2048, H=128, K=128, V=128, seed=20261208),

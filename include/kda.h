@@ -75,7 +75,18 @@ typedef struct kda_dims {
 size_t kda_fwd_workspace_size(const kda_dims* dims);
 
 /*
- * Full forward: kda_fwd_intra followed by kda_fwd_scan on the same stream.
+ * Full forward: kda_fwd_intra followed by kda_fwd_scan.  Every argument of
+ * both stages is checked before anything is launched.  One long sequence whose
+ * scan would leave most SMs idle (kda_workspace_layout's stage_count > 1, e.g.
+ * 32 heads x 65536 tokens at K = V = 128) runs as stage_count chunk ranges:
+ * the intra-chunk kernel of range j + 1 beside the scan of range j, on two
+ * streams the library creates once per device, forked from `stream` after the
+ * planner and joined back to it before the call returns (work enqueued on
+ * `stream` later runs after the whole forward; the fork and join are events,
+ * so the call can be captured in a CUDA graph).  Its results are bit for bit
+ * those of kda_fwd_intra followed by kda_fwd_scan (the state passes from
+ * range to range in fp32).  Calls of the staged path from several host threads
+ * are serialised while they enqueue.
  *
  *   q, k      bf16 [B, T, H, K]   queries / keys (the kernels do not normalise)
  *   v         bf16 [B, T, H, V]
@@ -108,7 +119,8 @@ kda_status kda_fwd_intra(const void* q, const void* k, const void* v, const floa
 /*
  * Inter-chunk stage alone: the serial state scan and the output, reading the
  * intermediates that kda_fwd_intra left in `workspace` for the same dims.
- * One CTA per (sequence, head, 64-wide V tile).
+ * One CTA per (sequence, head, V tile of 64 or 128 columns), serial over the
+ * sequence's chunks (or over a segment of them, for few sequences x heads).
  */
 kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const kda_dims* dims,
                         void* workspace, size_t workspace_bytes, void* stream);
@@ -311,6 +323,13 @@ typedef struct kda_ws_layout {
     int32_t seg_count;
     int32_t seg_len;
     size_t pq, hin;
+    /* Staged forward (one sequence whose scan leaves most SMs idle): kda_fwd
+     * runs the sequence as stage_count chunk ranges of stage_len chunks, the
+     * intra-chunk kernel of range j + 1 beside the scan of range j, and the
+     * scan passes its fp32 state from range to range through hin (fp32
+     * [stage_count, 1, H, K, V]).  stage_count = 1: not staged. */
+    int32_t stage_count;
+    int32_t stage_len;
 } kda_ws_layout;
 kda_status kda_workspace_layout(const kda_dims* dims, kda_ws_layout* out);
 

@@ -184,3 +184,30 @@ def test_segmented_scan_plan():
         assert (S - 1) * lay.seg_len < chunks <= S * lay.seg_len
         assert lay.hin - lay.pq == S * n * d.H * d.K * (d.K + d.V) * 4
         assert lay.total - lay.hin == S * n * d.H * d.K * d.V * 4
+
+
+def test_staged_forward_plan():
+    """One sequence whose scan would leave more than half of the SMs idle, and
+    that the segmented plan leaves whole, is run in chunk ranges of at least
+    64 chunks (at most 8 ranges); the state passes through the hin region."""
+    lay = kda.workspace_layout(kda.make_dims(1, 65536, 32, 128, 128))    # long: 64 scan CTAs
+    assert (lay.stage_count, lay.stage_len) == (8, 128)
+    assert lay.seg_count == 1 and lay.total - lay.hin == 8 * 32 * 128 * 128 * 4
+    lay = kda.workspace_layout(kda.make_dims(1, 12293, 32, 128, 128))    # 193 chunks
+    assert (lay.stage_count, lay.stage_len) == (3, 65)
+    lay = kda.workspace_layout(kda.make_dims(1, 9000, 32, 128, 128, num_seqs=1))  # one packed sequence
+    assert (lay.stage_count, lay.stage_len) == (2, 71)
+    for d in [kda.make_dims(4, 8192, 32, 128, 128),           # headline: four sequences
+              kda.make_dims(1, 9000, 32, 128, 128, num_seqs=2),
+              kda.make_dims(1, 8192, 80, 128, 128),            # 160 scan CTAs: no idle SMs
+              kda.make_dims(1, 8000, 32, 128, 128),            # 125 chunks: under two ranges
+              kda.make_dims(1, 65536, 32, 64, 64),             # segmented instead
+              kda.make_dims(1, 4096, 16, 128, 128)]:           # segmented instead
+        lay = kda.workspace_layout(d)
+        assert lay.stage_count == 1
+    for d in [kda.make_dims(1, 65536, 32, 128, 128), kda.make_dims(1, 8269, 32, 128, 128),
+              kda.make_dims(1, 8192, 64, 64, 64)]:
+        lay = kda.workspace_layout(d)
+        chunks = (d.T + 63) // 64  # every range holds at least one chunk, together all of them
+        assert lay.stage_len >= 64 and (lay.stage_count - 1) * lay.stage_len < chunks <= lay.stage_count * lay.stage_len
+        assert kda.workspace_size(d) == lay.total
