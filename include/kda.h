@@ -86,7 +86,8 @@ size_t kda_fwd_workspace_size(const kda_dims* dims);
  * so the call can be captured in a CUDA graph).  Its results are bit for bit
  * those of kda_fwd_intra followed by kda_fwd_scan (the state passes from
  * range to range in fp32).  Calls of the staged path from several host threads
- * are serialised while they enqueue.
+ * are serialised while they enqueue.  The first staged call on a device
+ * creates the two streams and their events: make it before any stream capture.
  *
  *   q, k      bf16 [B, T, H, K]   queries / keys (the kernels do not normalise)
  *   v         bf16 [B, T, H, V]
