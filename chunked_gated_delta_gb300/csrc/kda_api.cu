@@ -583,6 +583,61 @@ PipeRes* pipe_res() {
     return ok ? &r : nullptr;
 }
 
+// Fixed-length problems run kda_fwd_host as a pipeline over time slices: the
+// tokens are cut into `slices` ranges of whole 64-token chunks; slice j's
+// inputs (every sequence's rows of the range, one strided copy per tensor) go
+// host -> device on a copy stream while slice j - 1 computes on the caller's
+// stream and slice j - 2's outputs go device -> host on a second copy stream,
+// with two arena slots.  Slice j is kda_fwd on the sub-problem [B, T_j] whose
+// initial state is slice j - 1's final state (fp32, kept in the arena): the
+// chunks and the per-chunk arithmetic are those of one call over all T tokens,
+// so the results are the same bits.  Unlike head groups, every slice runs a
+// fraction of the serial scan, and only the first slice's copies and the last
+// slice's compute and output copies stay exposed.
+constexpr int kSliceMax = 8;
+
+bool use_slices(const kda_dims* d) {
+    return !is_varlen(d) && (int64_t)d->B * d->T >= kPipeMinRows && d->T >= 2 * kChunk;
+}
+
+struct SliceArena {
+    int slices, ts;  // slice count, tokens per slice (a multiple of 64; the last may be shorter)
+    size_t q, k, v, g, beta, o, slot_bytes;  // offsets inside a slot
+    size_t slot0, h0, state, ws, ws_bytes, total;
+};
+SliceArena slice_arena(const kda_dims* d) {
+    SliceArena A{};
+    const int64_t nt = ((int64_t)d->T + kChunk - 1) / kChunk;
+    const int64_t per = (nt + kSliceMax - 1) / kSliceMax;  // chunks per slice
+    A.ts = (int)(per * kChunk);
+    A.slices = (int)((nt + per - 1) / per);
+    const size_t rows = (size_t)d->B * A.ts, B = (size_t)d->B, H = (size_t)d->H, K = (size_t)d->K,
+                 V = (size_t)d->V;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 1024);
+        return at;
+    };
+    A.q = take(rows * H * K * 2);
+    A.k = take(rows * H * K * 2);
+    A.v = take(rows * H * V * 2);
+    A.g = take(rows * H * K * 4);
+    A.beta = take(rows * H * 2);
+    A.o = take(rows * H * V * 2);
+    A.slot_bytes = off;
+    off = 0;
+    A.slot0 = take(A.slot_bytes * 2);
+    A.h0 = take(B * H * K * V * 4);
+    A.state = take(2 * B * H * K * V * 4);  // two fp32 states, slice j writes state[j & 1]
+    kda_dims sd = *d;
+    sd.T = A.ts;  // the largest slice (workspace size grows with T)
+    A.ws_bytes = ws_layout(sd, false).total;
+    A.ws = take(A.ws_bytes);
+    A.total = off;
+    return A;
+}
+
 // rows x width bytes, source rows `src_pitch` apart, packed at dst (or the reverse)
 cudaError_t copy_rows(void* dst, size_t dst_pitch, const void* src, size_t src_pitch, size_t width, size_t rows,
                       cudaMemcpyKind kind, cudaStream_t s) {
@@ -590,10 +645,87 @@ cudaError_t copy_rows(void* dst, size_t dst_pitch, const void* src, size_t src_p
     if (dst_pitch == width && src_pitch == width) return cudaMemcpyAsync(dst, src, width * rows, kind, s);
     return cudaMemcpy2DAsync(dst, dst_pitch, src, src_pitch, width, rows, kind, s);
 }
+
+// Tokens [t0, t0 + tj) of every one of B sequences: host [B, T, tok] <-> device
+// [B, tj, tok] packed (tok = bytes per token).  One strided copy, or one copy
+// per sequence when the host pitch is 512 MiB or more (2-D copies take
+// pitches below that size here).
+cudaError_t copy_slice(uint8_t* dev, const uint8_t* host_in, uint8_t* host_out, size_t tok, size_t T, size_t t0,
+                       size_t tj, size_t B, cudaStream_t s) {
+    const size_t hp = T * tok, dp = tj * tok, w = tj * tok;
+    const bool up = host_in != nullptr;
+    if (hp < ((size_t)1 << 29)) {
+        return up ? copy_rows(dev, dp, host_in + t0 * tok, hp, w, B, cudaMemcpyHostToDevice, s)
+                  : copy_rows(host_out + t0 * tok, hp, dev, dp, w, B, cudaMemcpyDeviceToHost, s);
+    }
+    for (size_t b = 0; b < B; ++b) {
+        const cudaError_t e = up ? cudaMemcpyAsync(dev + b * dp, host_in + b * hp + t0 * tok, w,
+                                                   cudaMemcpyHostToDevice, s)
+                                 : cudaMemcpyAsync(host_out + b * hp + t0 * tok, dev + b * dp, w,
+                                                   cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+kda_status fwd_host_slices(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                           float scale, const float* h0, void* o, float* ht, const kda_dims* dims, uint8_t* base,
+                           cudaStream_t s) {
+    const SliceArena A = slice_arena(dims);
+    const size_t B = dims->B, T = dims->T, H = dims->H, K = dims->K, V = dims->V;
+    const size_t state_bytes = B * H * K * V * 4;
+    std::unique_lock<std::mutex> lock(g_pipe_mutex);
+    PipeRes* R = pipe_res();
+    // without the pipeline's streams every step runs in order on the caller's stream
+    cudaStream_t s_in = R ? R->in : s, s_out = R ? R->out : s;
+    auto wait = [&](cudaStream_t who, cudaEvent_t e) { return !R || cudaStreamWaitEvent(who, e, 0) == cudaSuccess; };
+    auto record = [&](cudaEvent_t e, cudaStream_t who) { return !R || cudaEventRecord(e, who) == cudaSuccess; };
+    if (R && (!record(R->start, s) || !wait(s_in, R->start) || !wait(s_out, R->start))) return KDA_ERR_CUDA;
+    bool ok = !h0 || cudaMemcpyAsync(base + A.h0, h0, state_bytes, cudaMemcpyHostToDevice, s_in) == cudaSuccess;
+    kda_status st = ok ? KDA_OK : KDA_ERR_CUDA;
+    for (int j = 0; j < A.slices && st == KDA_OK; ++j) {
+        const int slot = j & 1;
+        uint8_t* sb = base + A.slot0 + slot * A.slot_bytes;
+        const size_t t0 = (size_t)j * A.ts, tj = std::min<size_t>(A.ts, T - t0);
+        // inputs of slice j (slice j - 2 has computed and its outputs have left the slot)
+        ok = !(R && j >= 2) || wait(s_in, R->ev_out[slot]);
+        auto up = [&](size_t off, const void* src, size_t tok) {
+            return copy_slice(sb + off, static_cast<const uint8_t*>(src), nullptr, tok, T, t0, tj, B, s_in) ==
+                   cudaSuccess;
+        };
+        ok = ok && up(A.q, q, H * K * 2) && up(A.k, k, H * K * 2) && up(A.v, v, H * V * 2) && up(A.g, g, H * K * 4) &&
+             up(A.beta, beta, H * 2);
+        ok = ok && record(R ? R->ev_in[slot] : nullptr, s_in) && wait(s, R ? R->ev_in[slot] : nullptr);
+        if (!ok) {
+            st = KDA_ERR_CUDA;
+            break;
+        }
+        // slice j from slice j - 1's final state (or h0)
+        kda_dims sd = *dims;
+        sd.T = (int32_t)tj;
+        const float* h_in = j == 0 ? (h0 ? reinterpret_cast<const float*>(base + A.h0) : nullptr)
+                                   : reinterpret_cast<const float*>(base + A.state + ((j - 1) & 1) * state_bytes);
+        float* h_out = reinterpret_cast<float*>(base + A.state + (j & 1) * state_bytes);
+        st = kda_fwd(sb + A.q, sb + A.k, sb + A.v, reinterpret_cast<const float*>(sb + A.g), sb + A.beta, scale, h_in,
+                     nullptr, sb + A.o, h_out, &sd, base + A.ws, A.ws_bytes, s);
+        if (st != KDA_OK) break;
+        // outputs of slice j (and the final state after the last one)
+        ok = record(R ? R->ev_comp[slot] : nullptr, s) && wait(s_out, R ? R->ev_comp[slot] : nullptr) &&
+             copy_slice(sb + A.o, nullptr, static_cast<uint8_t*>(o), H * V * 2, T, t0, tj, B, s_out) == cudaSuccess;
+        if (ok && ht && j == A.slices - 1)
+            ok = cudaMemcpyAsync(ht, h_out, state_bytes, cudaMemcpyDeviceToHost, s_out) == cudaSuccess;
+        ok = ok && record(R ? R->ev_out[slot] : nullptr, s_out);
+        if (!ok) st = KDA_ERR_CUDA;
+    }
+    // the caller's stream completes after the last output copy (joined also after a failure)
+    if (R && (!record(R->done, s_out) || !wait(s, R->done)) && st == KDA_OK) st = KDA_ERR_CUDA;
+    return st;
+}
 }  // namespace
 
 size_t kda_fwd_host_arena_size(const kda_dims* dims) {
     if (!dims || check_dims(dims, is_varlen(dims)) != KDA_OK) return 0;
+    if (use_slices(dims)) return slice_arena(dims).total;
     return host_arena(dims).total;
 }
 
@@ -606,13 +738,14 @@ kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float
     if (varlen != (cu_seqlens != nullptr)) return KDA_ERR_INVALID_ARG;
     kda_status st = check_dims(dims, varlen);
     if (st != KDA_OK) return st;
-    const HostArena A = host_arena(dims);
-    if (!arena || !aligned(arena, 256) || arena_bytes < A.total) return KDA_ERR_WORKSPACE;
+    if (!arena || !aligned(arena, 256) || arena_bytes < kda_fwd_host_arena_size(dims)) return KDA_ERR_WORKSPACE;
     const size_t rows = (size_t)dims->B * dims->T;
     const size_t N = varlen ? (size_t)dims->num_seqs : (size_t)dims->B;
     if (rows > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(arena);
+    if (use_slices(dims)) return fwd_host_slices(q, k, v, g, beta, scale, h0, o, ht, dims, base, s);
+    const HostArena A = host_arena(dims);
     const size_t H = dims->H, K = dims->K, V = dims->V, hp = A.hp;
 
     std::unique_lock<std::mutex> lock(g_pipe_mutex);

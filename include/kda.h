@@ -222,9 +222,13 @@ kda_status kda_bwd_dh(float scale, const void* do_, const void* dv_in, const flo
  *   arena: device memory of at least kda_fwd_host_arena_size(dims) bytes,
  *   256-byte aligned, owned by the caller; it holds the device copies of the
  *   inputs and outputs and the workspace.
- *   Problems of 4096 rows (B * T) or more with an even head count run as a
- *   pipeline over two head groups: one group's host -> device copies overlap
- *   the other's kernels and device -> host copies, on two streams the library
+ *   Problems of 4096 rows (B * T) or more run as a pipeline: fixed-length
+ *   ones over up to 8 time slices of whole 64-token chunks (each slice a
+ *   kda_fwd over every sequence's rows of the slice, started from the
+ *   previous slice's fp32 final state kept in the arena: the same bits as one
+ *   kda_fwd), packed ones with an even head count over two head groups.  One
+ *   piece's host -> device copies overlap the previous piece's kernels and
+ *   the one before's device -> host copies, on two streams the library
  *   creates once per device (the call returns after enqueuing; `stream`
  *   completes when every copy has).  Calls are serialised internally.
  */

@@ -276,9 +276,11 @@ def test_bounded_wait_expires_and_context_survives():
 
 @pytest.mark.parametrize("shape", ["fixed", "varlen"])
 def test_host_entry_point_head_group_pipeline(shape):
-    """Problems of 4096+ rows run kda_fwd_host as a pipeline over head groups
-    (copies of one group overlap the compute of the previous one): the result
-    matches the oracle and the device entry point."""
+    """Problems of 4096+ rows run kda_fwd_host as a pipeline, over time slices
+    (fixed length) or head groups (packed): copies of one piece overlap the
+    compute of the previous one.  The result matches the oracle and the
+    device entry point (bit for bit for time slices: the same chunks, the
+    state handed on in fp32)."""
     import chunked_gated_delta_gb300 as kda
     if shape == "fixed":
         x = synth.make_inputs(make(B=2, T=2100, H=8, seed=91))
@@ -300,6 +302,43 @@ def test_host_entry_point_head_group_pipeline(shape):
     o_dev, ht_dev = run_gpu(x)
     torch.testing.assert_close(o.float(), o_dev.cpu().float(), rtol=2e-2, atol=2e-3)
     torch.testing.assert_close(ht, ht_dev.cpu(), rtol=1e-2, atol=1e-3)
+    if shape == "fixed":
+        assert torch.equal(o, o_dev.cpu()) and torch.equal(ht, ht_dev.cpu())
+
+
+def _host_call(x, want_ht=True):
+    import chunked_gated_delta_gb300 as kda
+    dims = kda.make_dims(x["B"], x["T"], x["H"], x["K"], x["V"])
+    arena = torch.empty(kda.host_arena_size(dims), dtype=torch.uint8, device="cuda")
+    pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    h0 = x["h0"].pin_memory() if x["h0"] is not None else None
+    o = torch.empty((x["B"], x["T"], x["H"], x["V"]), dtype=torch.bfloat16, pin_memory=True)
+    ht = torch.empty((x["B"], x["H"], x["K"], x["V"]), dtype=torch.float32, pin_memory=True) if want_ht else None
+    kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], x["scale"], h0, None, o, ht, dims, arena)
+    torch.cuda.synchronize()
+    return o, ht
+
+
+def test_host_time_slices_ragged_bitwise():
+    """Three sequences of 1537 tokens (a ragged last slice and chunk): kda_fwd_host
+    over time slices gives the bits of kda_fwd, with and without ht."""
+    x = synth.make_inputs(make(B=3, T=1537, H=32, seed=93))
+    o, ht = _host_call(x)
+    o_dev, ht_dev = run_gpu(x)
+    assert torch.equal(o, o_dev.cpu()) and torch.equal(ht, ht_dev.cpu())
+    o2, _ = _host_call(x, want_ht=False)
+    assert torch.equal(o2, o)
+
+
+def test_host_time_slices_long_sequence_bitwise():
+    """One 65536-token sequence of 32 heads (each slice itself staged on the
+    device; host rows of q, k, v, g, o of 512 MiB or more take one copy per
+    sequence): the bits of
+    kda_fwd."""
+    x = synth.make_inputs(synth.WORKLOADS["long"])
+    o, ht = _host_call(x)
+    o_dev, ht_dev = run_gpu(x)
+    assert torch.equal(o, o_dev.cpu()) and torch.equal(ht, ht_dev.cpu())
 
 
 def test_varlen_thousands_of_short_sequences():
