@@ -100,7 +100,11 @@ def ncu_traffic(kernel_name, src_file, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 25 ms while running.
+    Each line is stamped with the host clock on arrival; mark_start() and
+    mark_end() bracket the timed region, and the report takes the samples
+    that arrived inside it (or, for a region shorter than the sampling
+    interval, the first sample after it started)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -110,12 +114,13 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -125,7 +130,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
@@ -139,7 +150,12 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines, window = self.lines, "whole run"
+        if self.t0 is not None and self.t1 is not None:
+            inside = [x for x in lines if self.t0 <= x[0] <= self.t1 + 0.03]
+            after = [x for x in lines if x[0] >= self.t0][:1]
+            lines, window = (inside, "timed region") if inside else (after, "first sample after the region started")
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -153,7 +169,7 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "window": window, "reasons": sorted(reasons)}
 
 
 def host_cores():
@@ -292,11 +308,13 @@ def run_gb300(args):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     ev[0].record(stream)
     for i in range(args.steps):
         step()
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_end()
     barrier(world)
     clk = clocks.stop()
     total_ms = ev[0].elapsed_time(ev[1])
@@ -452,11 +470,13 @@ def run_gb300_bwd(args):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     ev[0].record(stream)
     for i in range(args.steps):
         step()
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_end()
     barrier(world)
     clk = clocks.stop()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
@@ -572,7 +592,9 @@ def run_e2e(args, kda, x, dims, stream, dev, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200 on the GPU, long enough for in-region clock samples; "
+                         "5 for the reference arm, whose steps are seconds of host work)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="headline")
@@ -583,6 +605,8 @@ def main():
     ap.add_argument("--path", choices=("fwd", "bwd_dh"), default="fwd",
                     help="fwd: the forward (default); bwd_dh: the reverse state scan")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 5 if args.impl == "reference" else 200
     if args.warmup < 3 and args.impl == "gb300":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
