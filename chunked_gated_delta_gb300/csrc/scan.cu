@@ -544,11 +544,16 @@ cudaError_t launch_scan_k(const ScanArgs& a, int mode, cudaStream_t stream, int 
 
 // Chains the segment maps of the map pass: for every (sequence, head, 16
 // columns of V), h_in[0] = h0 and h_in[j+1] = P_j h_in[j] + Q_j in fp32, for
-// the segments the sequence has.  Thread r owns state row r and its 16
-// columns.  P_j (K x K) streams into a double buffer by cp.async while the
+// the segments the sequence has.  Two threads per state row r (2K threads):
+// each sums the products over one half of the key dims for the row's 16
+// columns, and a lane exchange adds the halves, so a step's serial work is
+// half a row.  P_j (K x K) streams into a double buffer by cp.async while the
 // previous step computes; its rows keep their 16-byte chunks XOR-swizzled by
-// (row & 7), so the float4 row reads of 8 consecutive threads hit distinct
-// banks.  h_in[j] (K x 16) is double-buffered and read as broadcast float4s.
+// (row & 7), and the second half walks its chunks four places rotated, so the
+// two threads of a row read different banks.  h_in[j] (K x 16) is
+// double-buffered and read as broadcast float4s; the second half takes the
+// rows of each group of four in the order 1 0 3 2, so the two broadcast rows
+// of a warp never share a bank.
 constexpr int kCombineCols = 16;
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -559,10 +564,10 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int K>
-__global__ void __launch_bounds__(128) kda_seg_combine_kernel(const void* __restrict__ h0, uint8_t* __restrict__ ws,
-                                                              const WsLayout L, const int N, const int H, const int V,
-                                                              const int flags) {
-    constexpr int C = kCombineCols, K4 = K / 4;
+__global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __restrict__ h0, uint8_t* __restrict__ ws,
+                                                                const WsLayout L, const int N, const int H,
+                                                                const int V, const int flags) {
+    constexpr int C = kCombineCols, K4 = K / 4, HK4 = K4 / 2, NTH = 2 * K;
     extern __shared__ float4 csm4[];
     float4* Ps = csm4;              // 2 x [K][K / 4], chunk-swizzled rows
     float4* Hs = csm4 + 2 * K * K4;  // 2 x [K][C / 4]
@@ -575,21 +580,21 @@ __global__ void __launch_bounds__(128) kda_seg_combine_kernel(const void* __rest
     if (nseg < 2) return;
     const int tid = threadIdx.x;
     const int col0 = vt * C;
-    const int r = tid;  // state row
+    const int r = tid >> 1, half = tid & 1;  // state row, half of the key dims
     const float* pq = reinterpret_cast<const float*>(ws + L.pq);
     float* hin = reinterpret_cast<float*>(ws + L.hin);
     auto map_of = [&](int j) { return pq + (((int64_t)j * N + s) * H + h) * K * (K + V); };
     auto stage_p = [&](int j) {  // issue the copies of P_j into buffer j & 1
         const float* PQ = map_of(j);
         float4* dst = Ps + (j & 1) * K * K4;
-        for (int e4 = tid; e4 < K * K4; e4 += 128) {
+        for (int e4 = tid; e4 < K * K4; e4 += NTH) {
             const int row = e4 / K4, c4 = e4 % K4;
             cp_async16(dst + row * K4 + (c4 ^ (row & 7)), PQ + (int64_t)row * (K + V) + 4 * c4);
         }
         cp_async_commit();
     };
     stage_p(0);
-    if (r < K) {
+    if (half == 0) {
         float hr[C];
 #pragma unroll
         for (int c = 0; c < C; ++c) {
@@ -607,6 +612,10 @@ __global__ void __launch_bounds__(128) kda_seg_combine_kernel(const void* __rest
             Hs[r * (C / 4) + c4] = make_float4(hr[4 * c4], hr[4 * c4 + 1], hr[4 * c4 + 2], hr[4 * c4 + 3]);
     }
     for (int j = 0; j + 1 < nseg; ++j) {
+        // this thread's half of Q_j's row (columns 8 half .. + 7), fetched ahead of the sums
+        const float* qrow = map_of(j) + (int64_t)r * (K + V) + K + col0 + 8 * half;
+        const float4 qa = *reinterpret_cast<const float4*>(qrow);
+        const float4 qb = *reinterpret_cast<const float4*>(qrow + 4);
         if (j + 2 < nseg) {
             stage_p(j + 1);  // overlaps this step
             cp_async_wait<1>();
@@ -617,36 +626,42 @@ __global__ void __launch_bounds__(128) kda_seg_combine_kernel(const void* __rest
         const float4* P = Ps + (j & 1) * K * K4;
         const float4* Hc = Hs + (j & 1) * K * (C / 4);
         float4* Hn = Hs + ((j + 1) & 1) * K * (C / 4);
-        if (r < K) {
-            const float* PQ = map_of(j);
-            float acc[C];
-            const float* q = PQ + (int64_t)r * (K + V) + K + col0;
+        float acc[C];
 #pragma unroll
-            for (int c = 0; c < C; ++c) acc[c] = q[c];
+        for (int c = 0; c < C; ++c) acc[c] = 0.f;
 #pragma unroll 2
-            for (int k4 = 0; k4 < K4; ++k4) {
-                const float4 p4 = P[r * K4 + (k4 ^ (r & 7))];
-                const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+        for (int i = 0; i < HK4; ++i) {
+            const int k4 = half ? HK4 + ((i + 4) & (HK4 - 1)) : i;
+            const float4 p4 = P[r * K4 + (k4 ^ (r & 7))];
+            const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {
+                const int kx = kk ^ half;  // the second half takes rows 1 0 3 2
+                const float pv = half ? pk[kk ^ 1] : pk[kk];
 #pragma unroll
-                    for (int c4 = 0; c4 < C / 4; ++c4) {
-                        const float4 x = Hc[(4 * k4 + kk) * (C / 4) + c4];
-                        acc[4 * c4] = fmaf(pk[kk], x.x, acc[4 * c4]);
-                        acc[4 * c4 + 1] = fmaf(pk[kk], x.y, acc[4 * c4 + 1]);
-                        acc[4 * c4 + 2] = fmaf(pk[kk], x.z, acc[4 * c4 + 2]);
-                        acc[4 * c4 + 3] = fmaf(pk[kk], x.w, acc[4 * c4 + 3]);
-                    }
+                for (int c4 = 0; c4 < C / 4; ++c4) {
+                    const float4 x = Hc[(4 * k4 + kx) * (C / 4) + c4];
+                    acc[4 * c4] = fmaf(pv, x.x, acc[4 * c4]);
+                    acc[4 * c4 + 1] = fmaf(pv, x.y, acc[4 * c4 + 1]);
+                    acc[4 * c4 + 2] = fmaf(pv, x.z, acc[4 * c4 + 2]);
+                    acc[4 * c4 + 3] = fmaf(pv, x.w, acc[4 * c4 + 3]);
                 }
             }
-            float4* dst = reinterpret_cast<float4*>(hin + ((((int64_t)(j + 1) * N + s) * H + h) * K + r) * V + col0);
-#pragma unroll
-            for (int c4 = 0; c4 < C / 4; ++c4) {
-                const float4 x = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
-                Hn[r * (C / 4) + c4] = x;
-                dst[c4] = x;
-            }
         }
+        // both halves of the row, then this thread's 8 columns plus Q
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 1);
+        float a8[8];  // this thread's columns, selected without indexing acc at run time
+#pragma unroll
+        for (int c = 0; c < 8; ++c) a8[c] = half ? acc[8 + c] : acc[c];
+        const float4 x0 = make_float4(a8[0] + qa.x, a8[1] + qa.y, a8[2] + qa.z, a8[3] + qa.w);
+        const float4 x1 = make_float4(a8[4] + qb.x, a8[5] + qb.y, a8[6] + qb.z, a8[7] + qb.w);
+        Hn[r * (C / 4) + 2 * half] = x0;
+        Hn[r * (C / 4) + 2 * half + 1] = x1;
+        float4* dst = reinterpret_cast<float4*>(hin + ((((int64_t)(j + 1) * N + s) * H + h) * K + r) * V + col0 +
+                                                8 * half);
+        dst[0] = x0;
+        dst[1] = x1;
         __syncthreads();
     }
 }
@@ -659,7 +674,7 @@ cudaError_t launch_combine_k(const ScanArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t ctas = (int64_t)a.N * a.H * (a.V / kCombineCols);
     if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, 128, smem, stream>>>(a.h0, a.ws, a.L, a.N, a.H, a.V, a.flags);
+    kern<<<(unsigned)ctas, 2 * K, smem, stream>>>(a.h0, a.ws, a.L, a.N, a.H, a.V, a.flags);
     return cudaGetLastError();
 }
 

@@ -89,6 +89,48 @@ def test_near_full_forget_invariant():
     assert_within(compare(x, o, ht, o_ref, ht_ref), "g=-80")
 
 
+@pytest.mark.parametrize("K", [64, 128])
+def test_beta0_g0_keeps_the_state(K):
+    """beta = 0 and g = 0: nothing is written or forgotten, so ht = h0 exactly
+    (the state update adds exact zeros) and o_t = scale * h0^T q_t, up to the
+    bf16 copy of h0 the output product reads."""
+    x = synth.make_inputs(make(B=2, T=333, H=3, K=K, V=K, seed=35))
+    x["beta"] = torch.zeros_like(x["beta"])
+    x["g"] = torch.zeros_like(x["g"])
+    o, ht = run_gpu(x)
+    assert torch.equal(ht.cpu(), x["h0"])
+    want = x["scale"] * torch.einsum("bthk,bhkv->bthv", x["q"].double(), x["h0"].double())
+    got = o.double().cpu()
+    assert float((got - want).norm() / want.norm()) < 5e-3
+    o_ref, ht_ref = oracle_ref(x)
+    assert_within(compare(x, o, ht, o_ref, ht_ref), "beta=0, g=0")
+
+
+@pytest.mark.parametrize("K", [64, 128])
+def test_orthonormal_keys_recall(K):
+    """beta = 1, g = 0, h0 = 0 and K orthonormal keys (one per token, T = K):
+    the final state recalls every value, ht^T k_j = v_j, to the precision of
+    the bf16 keys and intermediates; and the result matches the oracle."""
+    T = K
+    x = synth.make_inputs(make(B=1, T=T, H=2, K=K, V=K, h0=False, seed=36))
+    gen = torch.Generator().manual_seed(37)
+    keys = []
+    for _ in range(2):
+        Qm, _ = torch.linalg.qr(torch.randn((K, K), generator=gen, dtype=torch.float64))
+        keys.append(Qm.T)  # rows orthonormal
+    x["k"] = torch.stack(keys, dim=1).unsqueeze(0).to(torch.bfloat16)  # [1, T, 2, K]
+    x["beta"] = torch.ones_like(x["beta"])
+    x["g"] = torch.zeros_like(x["g"])
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = oracle_ref(x)
+    assert_within(compare(x, o, ht, o_ref, ht_ref), "orthonormal recall")
+    for h in range(2):
+        kk = x["k"][0, :, h].double()                         # [T, K]
+        recall = (ht[0, h].double().cpu().T @ kk.T).T           # [T, V]
+        v = x["v"][0, :, h].double()
+        assert float((recall - v).norm() / v.norm()) < 3e-2, h
+
+
 # ------------------------------------------------------------------ named workloads
 
 def test_mid_workload_full():
