@@ -77,7 +77,8 @@ struct BwdCfg {
     static constexpr int REC_WARPS = 4 * NVB;
     static constexpr int TMA_WARP = REC_WARPS;
     static constexpr int MMA_WARP = REC_WARPS + 1;
-    static constexpr int THREADS = 32 * (REC_WARPS + 2);
+    static constexpr int STORE_WARP = REC_WARPS + 2;
+    static constexpr int THREADS = 32 * (REC_WARPS + 3);
     static constexpr uint32_t TMEM_COLS = NVB == 1 ? 256 : 512;
     static constexpr int MIN_CTAS = (NVB == 1 && STAGES == 1) ? 2 : 1;
     // one input stage
@@ -103,6 +104,7 @@ template <int STAGES>
 struct BwdBars {
     uint64_t full[STAGES], empty[STAGES];
     uint64_t h_ready, dv_full, vp_ready, upd_full;
+    uint64_t hs_free, vp_free;  // the store warp's copies have read the dh / dv2 operand copies
     uint64_t do_ready[STAGES];  // fp16 do converted to bf16 in the stage
     uint32_t tmem_slot;
     int abort_flag;
@@ -112,7 +114,8 @@ template <int KB, int NVB, int STAGES, bool F16>
 __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, NVB, STAGES>::MIN_CTAS)
     kda_bwd_dh_kernel(const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_qg,
                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_dvin, const void* __restrict__ dht,
+                      const __grid_constant__ CUtensorMap tm_dvin, const __grid_constant__ CUtensorMap tm_dv2,
+                      const __grid_constant__ CUtensorMap tm_dhck, const void* __restrict__ dht,
                       uint16_t* __restrict__ dhck, uint16_t* __restrict__ dv2, void* __restrict__ dh0,
                       uint8_t* __restrict__ ws, const WsLayout L, const float scale, const int N, const int H,
                       const int V, const int mode, const int flags) {
@@ -159,6 +162,8 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
         mbar_init(&B.dv_full, 1);
         mbar_init(&B.vp_ready, 2 * NVB);
         mbar_init(&B.upd_full, 1);
+        mbar_init(&B.hs_free, 1);
+        mbar_init(&B.vp_free, 1);
         for (int i = 0; i < STAGES; ++i) mbar_init(&B.do_ready[i], 1);
         B.abort_flag = 0;
         fence_mbar_init();
@@ -261,7 +266,9 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             const int st = it % STAGES;
             const uint32_t sp = (it / STAGES) & 1;
             uint8_t* stage = sm + st * S::STAGE;
-            // MMA operand: dh before this chunk's update, bf16
+            // MMA operand: dh before this chunk's update, bf16 (once the store
+            // warp's copy of the previous chunk's checkpoint has read it)
+            if (it > 0 && !wait(&B.hs_free, (it - 1) & 1)) break;
             if (has_row) {
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
@@ -273,17 +280,12 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.h_ready);
-            // the checkpoint leaves after the hand-off (off the MMA's path), read
-            // back from the operand copy (the DV MMA only reads it too)
-            if (has_row && dhck != nullptr && !map_mode) {
-                uint4* ck = reinterpret_cast<uint4*>(dhck + (((int64_t)(si.tile_base + c) * H + h) * K + r) * V + col);
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) ck[cc] = *reinterpret_cast<const uint4*>(hs + r * 128 + ((cc ^ (r & 7)) << 4));
-            }
+            // (the checkpoint leaves from this copy through the store warp)
             if (!wait(&B.full[st], sp)) break;
             if (quad < 2) {
                 // dv2[r, :] = DV[r, :] + dv_in[r, :], rows past the sequence end = 0
                 if (!wait(&B.dv_full, it & 1)) break;
+                if (it > 0 && !wait(&B.vp_free, (it - 1) & 1)) break;
                 tc_fence_after();
                 const int valid = min(64, si.len - c * 64);
                 const bool row_ok = r < valid;
@@ -314,8 +316,9 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.vp_ready);
-                // dv2 rows leave after the hand-off, read back from the operand copy
-                if (row_ok && !map_mode && !f16) {
+                // dv2 rows of a tail chunk leave after the hand-off, read back from
+                // the operand copy (full chunks leave through the store warp)
+                if (row_ok && !map_mode && !f16 && valid < 64) {
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) gdst[cc] = *reinterpret_cast<const uint4*>(vp + r * 128 + ((cc ^ (r & 7)) << 4));
                 }
@@ -425,6 +428,39 @@ __global__ void __launch_bounds__(BwdCfg<KB, NVB, STAGES>::THREADS, BwdCfg<KB, N
             }
             if (f16 && nit > 0 && !*abort_flag) convert_do(nit - 1);
         }
+    } else if (warp == S::STORE_WARP) {
+        // ================= stores through TMA =================
+        // Per chunk: the checkpoint (dh before the update, the bf16 operand copy
+        // in HS) and, for a full bf16 chunk, dv2 (the operand copy in VP) leave
+        // by TMA stores; once their shared-memory reads are done, hs_free and
+        // vp_free let the recurrence warps rewrite the copies.  Rows of a tail
+        // chunk past the sequence end belong to the next sequence, so a tail's
+        // dv2 rows are stored by the recurrence warps with a row mask.
+        if (lane == 0 && nit > 0) {
+            const bool ck = dhck != nullptr && !map_mode;
+            if (ck) prefetch_tmap(&tm_dhck);
+            if (!map_mode && !f16) prefetch_tmap(&tm_dv2);
+            for (int it = 0; it < nit && !*abort_flag; ++it) {
+                const int c = c_hi - 1 - it;
+                if (!wait(&B.h_ready, it & 1)) break;
+                if (ck) {
+                    const int blk = (si.tile_base + c) * H + h;  // below 2^25: the host bounds chunks * H * 64
+#pragma unroll
+                    for (int vb = 0; vb < NVB; ++vb) tma_store_3d(&tm_dhck, sm + S::HS + vb * S::HS_BLOCK, v0 + vb * 64, 0, blk);
+                }
+                if (!wait(&B.vp_ready, it & 1)) break;
+                if (!map_mode && !f16 && si.len - c * 64 >= 64) {
+#pragma unroll
+                    for (int vb = 0; vb < NVB; ++vb)
+                        tma_store_3d(&tm_dv2, sm + S::VP + vb * 8192, v0 + vb * 64, h, si.bos + c * 64);
+                }
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(&B.hs_free);
+                mbar_arrive(&B.vp_free);
+            }
+            bulk_wait_read0();
+        }
     } else if (warp == S::MMA_WARP) {
         // ================= tcgen05 issuer =================
         if (lane == 0) {
@@ -496,8 +532,9 @@ cudaError_t launch_bwd_f(const BwdArgs& a, int mode, cudaStream_t stream) {
     const int segs = mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
     if (ctas <= 0 || segs <= 0) return cudaSuccess;
     const dim3 grid((unsigned)ctas, (unsigned)segs);
-    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.dht, a.dhck, a.dv2,
-                                             a.dh0, a.ws, a.L, a.scale, a.N, a.H, a.V, mode, a.flags);
+    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_kg, a.tm_qg, a.tm_w, a.tm_do, a.tm_dvin, a.tm_dv2, a.tm_dhck,
+                                             a.dht, a.dhck, a.dv2, a.dh0, a.ws, a.L, a.scale, a.N, a.H, a.V, mode,
+                                             a.flags);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,8 @@ struct ScanArgs {
 struct BwdArgs {
     CUtensorMap tm_kg, tm_qg, tm_w;  // workspace tiles, 2-D {dim, tiles*64}
     CUtensorMap tm_do, tm_dvin;      // user tensors, 3-D {V, H, rows}
+    CUtensorMap tm_dv2;              // dv2 (stores), 3-D {V, H, rows}
+    CUtensorMap tm_dhck;             // checkpoints (stores), 3-D {V, K, chunks * H}
     const void* dht;    // fp32 (or bf16) [N, H, K, V] or null
     uint16_t* dhck;     // bf16 [chunks, H, K, V] or null
     uint16_t* dv2;      // bf16 (or fp16) [rows, H, V]

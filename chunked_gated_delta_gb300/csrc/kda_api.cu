@@ -449,6 +449,14 @@ kda_status kda_bwd_dh_ex(float scale, const void* do_, const void* dv_in, const 
         ok = ok && map2(&a.tm_w, ws + L.w, dims->K, trows);
         ok = ok && map3(&a.tm_do, io, 2, do_, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         ok = ok && map3(&a.tm_dvin, io, 2, dv_in, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && map3(&a.tm_dv2, io, 2, dv2, dims->V, dims->H, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (dhck) {  // [chunks * H] blocks of K rows x V columns; a box is one block's 64 columns
+            const uint64_t cdims[3] = {(uint64_t)dims->V, (uint64_t)dims->K, (uint64_t)(L.max_chunks * dims->H)};
+            const uint64_t cstr[2] = {(uint64_t)dims->V * 2, (uint64_t)dims->K * dims->V * 2};
+            const uint32_t cbox[3] = {64, (uint32_t)dims->K, 1};
+            ok = ok && make_tensormap(&a.tm_dhck, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dhck, cdims, cstr, cbox,
+                                      CU_TENSOR_MAP_SWIZZLE_128B);
+        }
         if (!ok) return KDA_ERR_CUDA;
     }
     a.dht = dht;
