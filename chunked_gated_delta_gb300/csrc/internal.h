@@ -35,6 +35,7 @@ constexpr int kScanExitToHin = 4;   // output mode: a segment that ends before i
 
 struct ScanArgs {
     CUtensorMap tm_w, tm_qg, tm_kg, tm_u, tm_aqk;  // workspace tiles, 2-D {dim, tiles*64}
+    CUtensorMap tm_o;                              // o (stores), 3-D {V, H, rows}
     const void* h0;   // fp32 (or bf16) [N, H, K, V] or null
     void* ht;         // fp32 (or bf16) [N, H, K, V] or null
     uint16_t* o;      // bf16 (or fp16) bits [rows, H, V]

@@ -301,6 +301,15 @@ kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_
         ok = ok && map2(&a->tm_kg, ws + L.kg, dims->K, trows);
         ok = ok && map2(&a->tm_u, ws + L.u, dims->V, trows);
         ok = ok && map2(&a->tm_aqk, ws + L.aqk, kChunk, trows);
+        if (rows > 0) {  // o [rows, H, V]: a box is 32 token rows of one head's 64 columns
+            const uint64_t odims[3] = {(uint64_t)dims->V, (uint64_t)dims->H, (uint64_t)rows};
+            const uint64_t ostr[2] = {(uint64_t)dims->V * 2, (uint64_t)dims->V * 2 * dims->H};
+            const uint32_t obox[3] = {64, 1, 32};
+            ok = ok && make_tensormap(&a->tm_o,
+                                      op.io_dtype == KDA_IO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                      3, o, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
         if (!ok) return KDA_ERR_CUDA;
     }
     a->h0 = h0;

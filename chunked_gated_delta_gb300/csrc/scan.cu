@@ -75,8 +75,7 @@ struct ScanCfg {
     static constexpr uint32_t AQK = AW + 2 * KB * 8192;  // Aqk [64][64]; the 8K before it = rows 64..
     static constexpr uint32_t KG = AQK + 8192;           // kg per kb [64 tok][64 d]
     static constexpr uint32_t U = KG + KB * 8192;        // u per V block [64 tok][64 v]
-    static constexpr uint32_t GD = U + NVB * 8192;       // gd fp32 [K]
-    static constexpr uint32_t STAGE = GD + 1024;
+    static constexpr uint32_t STAGE = U + NVB * 8192;
     static constexpr uint32_t TX_BYTES = (3 * KB + 1 + NVB) * 8192 + K * 4;
     // persistent
     static constexpr uint32_t HS = STAGES * STAGE;       // h bf16 per V block [K rows][64 v], MN-major SW128
@@ -84,7 +83,14 @@ struct ScanCfg {
     static constexpr uint32_t VP = HS + NVB * HS_BLOCK;  // v' bf16 per V block [64 tok][64 v], MN-major SW128
     // [I_64 ; 0] bf16, K-major SW128 [128 rows][64 tok]: the A operand that puts u into the accumulator
     static constexpr uint32_t IDN = VP + NVB * 8192;
-    static constexpr uint32_t BYTES = IDN + 16384;
+    static constexpr uint32_t GDS = IDN + 16384;         // gd fp32 [K] of each ring stage (stage st at GDS + st * 4K)
+    // o leaves by TMA stores from a staging copy [64 tok][64 v] (SW128) per V
+    // block, each epilogue warp storing its own 32 rows (a tail's partial rows
+    // leave from registers); the two-CTAs-per-SM shape (one stage) has no
+    // room for it and stores every row from registers
+    static constexpr bool TMA_O = STAGES == 2;
+    static constexpr uint32_t OST = (GDS + STAGES * K * 4 + 1023) / 1024 * 1024;
+    static constexpr uint32_t BYTES = TMA_O ? OST + NVB * 8192 : GDS + STAGES * K * 4;
 };
 
 template <int STAGES>
@@ -108,7 +114,8 @@ template <int KB, int NVB, int STAGES>
 __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB, NVB, STAGES>::MIN_CTAS)
     kda_scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_qg,
                     const __grid_constant__ CUtensorMap tm_kg, const __grid_constant__ CUtensorMap tm_u,
-                    const __grid_constant__ CUtensorMap tm_aqk, const void* __restrict__ h0,
+                    const __grid_constant__ CUtensorMap tm_aqk, const __grid_constant__ CUtensorMap tm_o,
+                    const void* __restrict__ h0,
                     void* __restrict__ ht, uint16_t* __restrict__ o, uint8_t* __restrict__ ws,
                     const WsLayout L, const float scale, const int N, const int H, const int V, const int flags,
                     const int mode, const int seg_base) {
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.vp_ready);
             }
-            const float decay = has_row ? ex2(reinterpret_cast<const float*>(stage + S::GD)[r]) : 0.f;
+            const float decay = has_row ? ex2(reinterpret_cast<const float*>(sm + S::GDS + st * K * 4)[r]) : 0.f;
             if (!wait(&B.dh_full, it & 1)) break;
             tc_fence_after();
             if (has_row) {
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                     if (!map_mode) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, cb, row);
                     else if (cb >= K) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, cb - K, row);
                 }
-                bulk_load_1d(stage + S::GD, gd + tile * K, K * 4, fb);
+                bulk_load_1d(sm + S::GDS + st * K * 4, gd + tile * K, K * 4, fb);
             }
         }
     } else if (warp == S::MMA_WARP) {
@@ -463,26 +470,44 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 if (lane == 0) mbar_arrive(&B.acc_empty[buf]);
                 const int valid = min(64, si.len - c * 64);
                 const float nscale = -scale;  // the accumulator holds -(qg@h + Aqk@v')
-                if (i < valid) {
+                uint4 packed[8];  // this token row's 64 outputs, scaled and rounded
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float* y = acc + 8 * j;
+                    packed[j] = (flags & kScanOutF16)
+                                    ? make_uint4(pack_f16x2(nscale * y[0], nscale * y[1]),
+                                                 pack_f16x2(nscale * y[2], nscale * y[3]),
+                                                 pack_f16x2(nscale * y[4], nscale * y[5]),
+                                                 pack_f16x2(nscale * y[6], nscale * y[7]))
+                                    : make_uint4(pack_bf16x2(nscale * y[0], nscale * y[1]),
+                                                 pack_bf16x2(nscale * y[2], nscale * y[3]),
+                                                 pack_bf16x2(nscale * y[4], nscale * y[5]),
+                                                 pack_bf16x2(nscale * y[6], nscale * y[7]));
+                }
+                const int row_lo = (quad - 2) * 32;  // this warp's 32 token rows
+                if (S::TMA_O && valid >= row_lo + 32) {
+                    // all 32 rows real: into this warp's staging copy, then one TMA
+                    // store issued by lane 0 once its previous store has read the copy
+                    uint8_t* stg = sm + S::OST + vb * 8192 + row_lo * 128;
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = packed[j];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_o, stg, v0 + vb * 64, h, si.bos + c * 64 + row_lo);
+                        bulk_commit();
+                    }
+                } else if (i < valid) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         o + ((int64_t)(si.bos + c * 64 + i) * H + h) * V + v0 + vb * 64);
-                    if (flags & kScanOutF16) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_uint4(pack_f16x2(nscale * acc[8 * j], nscale * acc[8 * j + 1]),
-                                                pack_f16x2(nscale * acc[8 * j + 2], nscale * acc[8 * j + 3]),
-                                                pack_f16x2(nscale * acc[8 * j + 4], nscale * acc[8 * j + 5]),
-                                                pack_f16x2(nscale * acc[8 * j + 6], nscale * acc[8 * j + 7]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_uint4(pack_bf16x2(nscale * acc[8 * j], nscale * acc[8 * j + 1]),
-                                                pack_bf16x2(nscale * acc[8 * j + 2], nscale * acc[8 * j + 3]),
-                                                pack_bf16x2(nscale * acc[8 * j + 4], nscale * acc[8 * j + 5]),
-                                                pack_bf16x2(nscale * acc[8 * j + 6], nscale * acc[8 * j + 7]));
-                    }
+                    for (int j = 0; j < 8; ++j) dst[j] = packed[j];
                 }
             }
+            if (S::TMA_O && lane == 0) bulk_wait_read0();  // the staging outlives the stores' reads
         }
     }
 
@@ -523,7 +548,7 @@ cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream, int 
         flags |= kScanExitToHin;
     }
     const dim3 grid((unsigned)ctas, (unsigned)segs);
-    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.h0, a.ht, a.o, a.ws,
+    kern<<<grid, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.tm_o, a.h0, a.ht, a.o, a.ws,
                                              L, a.scale, a.N, a.H, a.V, flags, mode, stage >= 0 ? stage : 0);
     return cudaGetLastError();
 }
