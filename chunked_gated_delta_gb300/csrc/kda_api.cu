@@ -275,9 +275,9 @@ kda_status intra_impl(const void* q, const void* k, const void* v, const float* 
     return launch_intra(a, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-// Validation and TMA descriptors of the scan stage.  Launches nothing.
-kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
-                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, ScanArgs* a) {
+// Argument checks of the scan stage (no driver call).
+kda_status scan_check(const void* h0, void* o, void* ht, const kda_dims* dims, const kda_fwd_opts* opts,
+                      void* workspace, size_t workspace_bytes) {
     if (!dims) return KDA_ERR_INVALID_ARG;
     kda_fwd_opts op{};
     if (opts) op = *opts;
@@ -292,6 +292,19 @@ kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_
     if (rows > 0 && !o) return KDA_ERR_INVALID_ARG;
     if ((o && !aligned(o, 16)) || (h0 && !aligned(h0, 16)) || (ht && !aligned(ht, 16)))
         return KDA_ERR_ALIGNMENT;
+    return KDA_OK;
+}
+
+// Validation and TMA descriptors of the scan stage.  Launches nothing.
+kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
+                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, ScanArgs* a) {
+    kda_status st = scan_check(h0, o, ht, dims, opts, workspace, workspace_bytes);
+    if (st != KDA_OK) return st;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    const bool varlen = is_varlen(dims);
+    const WsLayout L = ws_layout(*dims, varlen);
+    const int64_t rows = (int64_t)dims->B * dims->T;
     *a = ScanArgs{};
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const int64_t trows = L.max_chunks * dims->H * kChunk;
@@ -493,10 +506,12 @@ kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* 
                       float scale, const void* h0, const int32_t* cu_seqlens, void* o, void* ht,
                       const kda_dims* dims, const kda_fwd_opts* opts, void* workspace,
                       size_t workspace_bytes, void* stream) {
-    // every argument of both stages is checked before anything is launched
+    // every argument of both stages is checked before any driver call or launch
+    kda_status st = scan_check(h0, o, ht, dims, opts, workspace, workspace_bytes);
+    if (st != KDA_OK) return st;
     IntraArgs ia;
     bool run = false;
-    kda_status st = intra_setup(q, k, v, g, beta, dims ? dims->H : 0, 0, cu_seqlens, dims, opts, workspace,
+    st = intra_setup(q, k, v, g, beta, dims ? dims->H : 0, 0, cu_seqlens, dims, opts, workspace,
                                 workspace_bytes, &ia, &run);
     if (st != KDA_OK) return st;
     ScanArgs sa;

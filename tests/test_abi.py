@@ -211,3 +211,24 @@ def test_staged_forward_plan():
         chunks = (d.T + 63) // 64  # every range holds at least one chunk, together all of them
         assert lay.stage_len >= 64 and (lay.stage_count - 1) * lay.stage_len < chunks <= lay.stage_count * lay.stage_len
         assert kda.workspace_size(d) == lay.total
+
+
+def test_staged_and_host_slice_paths_validate_before_any_launch(lib):
+    """The staged forward and the time-slice host pipeline check every argument
+    of both stages before anything is enqueued: on this machine (no GPU) any
+    launch would fail with KDA_ERR_CUDA, so argument errors must come first."""
+    d = kda.make_dims(1, 65536, 32, 128, 128)                           # staged (8 chunk ranges)
+    assert kda.workspace_layout(d).stage_count == 8
+    assert call_fwd(lib, d, q=FAKE + 8) == 3                            # misaligned q
+    assert call_fwd(lib, d, o=0) == 1                                   # no o (a scan-stage argument)
+    assert call_fwd(lib, d, o=FAKE + 4) == 3                            # misaligned o
+    assert call_fwd(lib, d, ws_bytes=kda.workspace_size(d) - 1) == 4    # one byte short (hin included)
+    P = ctypes.c_void_p
+    h = kda.make_dims(4, 8192, 32, 128, 128)                            # host pipeline over time slices
+    need = kda.host_arena_size(h)
+    host = ctypes.create_string_buffer(64)
+    args = [P(ctypes.addressof(host))] * 5
+    assert lib.kda_fwd_host(*args, ctypes.c_float(0.1), None, None, P(ctypes.addressof(host)), None,
+                            ctypes.byref(h), P(FAKE), ctypes.c_size_t(need - 1), None) == 4
+    assert lib.kda_fwd_host(*args, ctypes.c_float(0.1), None, None, None, None,
+                            ctypes.byref(h), P(FAKE), ctypes.c_size_t(need), None) == 1  # no o
