@@ -23,6 +23,9 @@
 //                      fp16 gradients the warp also rewrites each landed do
 //                      tile as bf16 for the qg^T @ do product.
 //   next warp          tcgen05 issuer + TMEM owner.
+//   next warp          TMA stores: each chunk's checkpoint from the bf16 dh
+//                      copy and, for a full chunk, dv2 from its bf16 copy;
+//                      then it releases both copies for the next chunk.
 // MMAs, all M = 128:
 //   DV  = [I ; *] @ dv_in     TMEM lanes 0-63 = dv_in exactly (lanes 64-127 unused)
 //   DV += [kg ; qg] @ dh      lanes 0-63 = dv2 before rounding

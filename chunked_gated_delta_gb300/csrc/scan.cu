@@ -16,7 +16,9 @@
 //   next warp          TMA producer: w, qg, kg, Aqk (shared by every V block),
 //                      u (this V tile) and gd per chunk into a STAGES-deep ring.
 //   next warp          tcgen05 issuer + TMEM owner.
-//   2*NVB warps        epilogue (TMEM quadrants 2-3): o rows, scaled, bf16.
+//   2*NVB warps        epilogue (TMEM quadrants 2-3): o rows, scaled, bf16,
+//                      staged in shared memory and sent 32 rows per warp by
+//                      TMA stores (a tail's partial rows from registers).
 // Every MMA uses M = 128 (one TMEM lane per accumulator row):
 //   ACC[buf]  = [I ; 0] @ u            lanes 0-63 = u (exact), 64-127 = 0
 //   ACC[buf] += -[w ; qg] @ h          lanes 0-63 = u - WH = v', 64-127 = -qg@h
