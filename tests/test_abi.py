@@ -232,3 +232,47 @@ def test_staged_and_host_slice_paths_validate_before_any_launch(lib):
                             ctypes.byref(h), P(FAKE), ctypes.c_size_t(need - 1), None) == 4
     assert lib.kda_fwd_host(*args, ctypes.c_float(0.1), None, None, None, None,
                             ctypes.byref(h), P(FAKE), ctypes.c_size_t(need), None) == 1  # no o
+
+
+def test_workspace_regions_hold_what_the_kernels_write():
+    """For a seeded spread of shapes (fixed length and packed, K and V of 64 and
+    128, short to long, few to many heads), the workspace regions are aligned,
+    in order, disjoint, and each is at least as large as what the kernels
+    index in it: the chunk table, gd, qg, kg, w, u, Aqk per (chunk, head)
+    tile, the segment maps [P | Q], and the entry states of the segments or
+    the chunk ranges of the staged forward."""
+    import random
+    rng = random.Random(20261202)
+    cases = [(4, 8192, 32, 128, 128, 0), (1, 65536, 32, 128, 128, 0), (1, 65536, 32, 64, 64, 0),
+             (1, 4096, 16, 128, 128, 0), (1, 9000, 32, 128, 128, 1), (1, 10049, 2, 128, 128, 5)]
+    for _ in range(200):
+        K, V = rng.choice((64, 128)), rng.choice((64, 128))
+        if rng.random() < 0.5:
+            cases.append((rng.randint(1, 8), rng.randint(0, 40000), rng.randint(1, 96), K, V, 0))
+        else:
+            n = rng.randint(1, 40)
+            cases.append((1, rng.randint(0, 60000), rng.randint(1, 96), K, V, n))
+    for B, T, H, K, V, ns in cases:
+        d = kda.make_dims(B, T, H, K, V, ns)
+        L = kda.workspace_layout(d)
+        names = ["status", "seq_info", "chunk_info", "gd", "qg", "kg", "w", "u", "aqk", "pq", "hin", "total"]
+        offs = [getattr(L, n) for n in names]
+        assert offs == sorted(offs), (B, T, H, K, V, ns)
+        assert all(o % 256 == 0 for o in offs[:3]) and all(o % 1024 == 0 for o in offs[3:-1])
+        N = ns if ns > 0 else B
+        nc = L.max_chunks
+        assert nc == ((T + 63 * N) // 64 if ns > 0 else B * ((T + 63) // 64))
+        tiles = nc * H
+        need = {"seq_info": 16 * max(N, 1), "chunk_info": 8 * max(nc, 1), "gd": tiles * K * 4,
+                "qg": tiles * 64 * K * 2, "kg": tiles * 64 * K * 2, "w": tiles * 64 * K * 2,
+                "u": tiles * 64 * V * 2, "aqk": tiles * 64 * 64 * 2}
+        for i, n in enumerate(names[1:-3], start=1):
+            assert offs[i + 1] - offs[i] >= need[n], (n, B, T, H, K, V, ns)
+        seg_units = L.seg_count * N * H if L.seg_count > 1 else 0
+        stage_units = L.stage_count * N * H if L.stage_count > 1 else 0
+        assert L.hin - L.pq >= seg_units * K * (K + V) * 4
+        assert L.total - L.hin >= max(seg_units, stage_units) * K * V * 4
+        assert not (L.seg_count > 1 and L.stage_count > 1)
+        if L.stage_count > 1:
+            assert N == 1 and (L.stage_count - 1) * L.stage_len < (T + 63) // 64 <= L.stage_count * L.stage_len
+        assert kda.workspace_size(d) == L.total
