@@ -4,7 +4,14 @@
 A step is one full forward through the C ABI (kda_fwd: chunk planner +
 intra-chunk kernel + scan kernel) over the headline workload (B=4, H=32, T=8192, K=V=128, bf16 I/O, fp32
 state), inputs resident in HBM.  The inputs (1.6 GB) are larger than L2, so
-no flush is done between steps.
+no flush is done between steps.  Every step has its own CUDA events; the line
+reports the median (the value), p10 and p90.  After the timed region a
+labelled clock-only window of untimed steps (about 0.5 s) gives the clock
+sampler several samples however short the timed region is.  The line also
+carries both HBM fractions of the step (two-stage algorithmic bytes and the
+strict single-pass I/O), the mid, varlen and long workloads timed in the same
+run (``other_workloads``; --no-configs skips them) and, from the CPU-baseline
+leg, the smoke-size parity figures against the fp64 oracle.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--path fwd|bwd_dh] [--workload NAME]
@@ -101,20 +108,23 @@ def ncu_traffic(kernel_name, src_file, workload):
 
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 25 ms while running.
-    Each line is stamped with the host clock on arrival; mark_start() and
-    mark_end() bracket the timed region, and the report takes the samples
-    that arrived inside it (or, for a region shorter than the sampling
-    interval, the first sample after it started)."""
+    Each line is stamped with the host clock on arrival.  mark_start() /
+    mark_end() bracket the timed region; mark_window() brackets a clock-only
+    window of back-to-back untimed steps run after it (a timed region of a
+    few milliseconds can fall between two samples).  stop() waits until a
+    sample stamped after the last mark has arrived, then reports the samples
+    inside the timed region and inside the window separately."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SLACK = 0.03  # a sample arriving this soon after a mark was taken before it
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.thread = None
-        self.t0 = self.t1 = None
+        self.t0 = self.t1 = self.w0 = self.w1 = None
 
     def start(self):
         try:
@@ -138,23 +148,13 @@ class ClockSampler:
     def mark_end(self):
         self.t1 = time.monotonic()
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
+    def mark_window(self, w0, w1):
+        self.w0, self.w1 = w0, w1
+
+    @staticmethod
+    def parse(lines):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lines, window = self.lines, "whole run"
-        if self.t0 is not None and self.t1 is not None:
-            inside = [x for x in lines if self.t0 <= x[0] <= self.t1 + 0.03]
-            after = [x for x in lines if x[0] >= self.t0][:1]
-            lines, window = (inside, "timed region") if inside else (after, "first sample after the region started")
         for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
@@ -167,9 +167,82 @@ class ClockSampler:
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        return sm, smax, reasons
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["nvidia-smi unavailable"]}
+        last = max([t for t in (self.t1, self.w1) if t is not None], default=None)
+        deadline = time.monotonic() + 2.0
+        while last is not None and time.monotonic() < deadline and not any(t > last + self.SLACK
+                                                                            for t, _ in self.lines):
+            time.sleep(0.01)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        lines = list(self.lines)
+        region = [x for x in lines if self.t0 is not None and self.t0 <= x[0] <= self.t1 + self.SLACK]
+        window = [x for x in lines if self.w0 is not None and self.w0 <= x[0] <= self.w1 + self.SLACK]
+        after = [x for x in lines if self.t1 is not None and x[0] > self.t1 + self.SLACK][:1]
+        sm_r, smax_r, why_r = self.parse(region)
+        sm_w, smax_w, why_w = self.parse(window)
+        sm_a, smax_a, why_a = self.parse(after)
+        if sm_r:
+            used, which = sm_r, "timed region"
+        elif sm_w:
+            used, which = sm_w, "clock window (untimed back-to-back steps right after the timed region)"
+        else:
+            used, which = sm_a, "first sample after the timed region"
+        smax = smax_r + smax_w + smax_a
+        return {"sm_mhz": statistics.median(used) if used else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "window": window, "reasons": sorted(reasons)}
+                "samples": len(used), "window": which,
+                "samples_in_region": len(sm_r), "sm_mhz_in_region": statistics.median(sm_r) if sm_r else None,
+                "samples_clock_window": len(sm_w),
+                "sm_mhz_clock_window": statistics.median(sm_w) if sm_w else None,
+                "clock_window_s": (self.w1 - self.w0) if self.w0 is not None else None,
+                "reasons": sorted(why_r | why_w | why_a)}
+
+
+def time_steps(step, n, stream):
+    """Runs n steps with a CUDA event between consecutive steps on `stream`;
+    returns (per-step ms list, first-to-last span ms)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for i in range(n):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)], ev[0].elapsed_time(ev[-1])
+
+
+def pct(xs, q):
+    """The q-quantile (0..1) of xs by linear interpolation."""
+    ys = sorted(xs)
+    if not ys:
+        return None
+    pos = q * (len(ys) - 1)
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
+def clock_window(step, ms_per_step, clocks, seconds=0.5):
+    """Untimed back-to-back steps for about `seconds` of GPU time, bracketed
+    for the clock sampler (outside the timed region)."""
+    import torch
+    n = max(1, int(seconds * 1e3 / max(ms_per_step, 1e-3)) + 1)
+    w0 = time.monotonic()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    clocks.mark_window(w0, time.monotonic())
+    return n
 
 
 def host_cores():
@@ -254,6 +327,104 @@ def launches_per_step(lay):
     return 3 + (2 if lay.seg_count > 1 else 0)
 
 
+def strict_bytes_per_token_head(K, V):
+    """Bytes per token-head a single-pass forward must move: read q, k, v, g,
+    beta once and write o once (the intermediates never leave the chip)."""
+    return 2 * K * 2 + V * 2 + K * 4 + 2 + V * 2
+
+
+def step_roofline(K, V, tokens_heads, state_bytes, ms, hbm, tc):
+    """Both HBM bounds of one forward (two-stage algorithmic bytes, and the
+    strict single-pass I/O) and the tensor-core time, with the fractions a
+    step of `ms` milliseconds reaches."""
+    b_intra, b_scan = bytes_per_token_head(K, V)
+    two = (b_intra + b_scan) * tokens_heads + state_bytes
+    strict = strict_bytes_per_token_head(K, V) * tokens_heads + state_bytes
+    flops = flops_per_token_head(K, V) * tokens_heads
+    two_ms = two / (hbm * 1e9) * 1e3
+    strict_ms = strict / (hbm * 1e9) * 1e3
+    return {"bytes": two, "hbm_ms": two_ms, "frac_of_hbm_bound": two_ms / ms,
+            "strict_io_bytes": strict, "strict_io_hbm_ms": strict_ms, "frac_of_strict_io_bound": strict_ms / ms,
+            "flops": flops, "tc_ms": flops / (tc * 1e12) * 1e3}
+
+
+def measure_workload(kda, name, dev, steps, hbm, tc):
+    """One extra workload's forward timed in the same run (inputs drawn on the
+    device, same distributions; its own warm-up): median and p10/p90 per step
+    and its roofline fractions."""
+    import torch
+    from chunked_gated_delta_gb300 import synth
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs_on(w, dev)
+    B, T, H, K, V, N = x["B"], x["T"], x["H"], x["K"], x["V"], x["N"]
+    dims = kda.make_dims(B, T, H, K, V, 0 if x["cu_seqlens"] is None else N)
+    ws = kda.new_workspace(dims, dev)
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"], cu_seqlens=x["cu_seqlens"],
+                workspace=ws, out=o, final_state=ht, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    if kda.status(ws, stream) != 0:
+        raise RuntimeError(f"kernel status on {name}")
+    per, _ = time_steps(step, steps, stream)
+    med = statistics.median(per)
+    tokens = B * T
+    hstate = (2 if x["h0"] is not None else 1) * N * H * K * V * 4
+    lay = kda.workspace_layout(dims)
+    out = {"workload": workload_config(w, x)["workload"], "steps": steps, "ms_per_step": med,
+           "ms_p10": pct(per, 0.1), "ms_p90": pct(per, 0.9), "tokens_per_s": tokens / (med / 1e3),
+           "launches_per_step": launches_per_step(lay), "plan": plan_name(lay),
+           "step_roofline": step_roofline(K, V, tokens * H, hstate, med, hbm, tc)}
+    del x, ws, o, ht
+    torch.cuda.empty_cache()
+    return out
+
+
+def plan_name(lay):
+    if lay.stage_count > 1:
+        return f"staged ({lay.stage_count} chunk ranges of {lay.stage_len})"
+    if lay.seg_count > 1:
+        return f"segmented scan ({lay.seg_count} segments of {lay.seg_len} chunks)"
+    return "two-stage (intra kernel, then scan)"
+
+
+def gpu_parity_small(kda, dev):
+    """GPU results of the smoke-size problems whose parity the CPU-baseline
+    leg reports: the tiny workload and a two-sequence K = V = 128 problem."""
+    import torch
+    from chunked_gated_delta_gb300 import synth
+    out = {}
+    for name, w in (("tiny", synth.WORKLOADS["tiny"]),
+                    ("smoke", synth.Workload("smoke", B=2, T=150, H=2, K=128, V=128, seed=7))):
+        x = synth.make_inputs(w)
+        d = {n: (x[n].to(dev) if isinstance(x[n], torch.Tensor) else x[n]) for n in x}
+        o, ht = kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"])
+        torch.cuda.synchronize(dev)
+        out[name] = (x, o.cpu(), ht.cpu())
+    return out
+
+
+def parity_figures(small):
+    """Errors of the GPU results against the fp64 oracle (the tolerances the
+    tests hold: rel_o, rel_ht <= 5e-3, maxrel_o <= 2e-2)."""
+    import numpy as np
+    import oracle
+    res = {}
+    for name, (x, o, ht) in small.items():
+        o_ref, ht_ref = oracle.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"])
+        og = o.double().numpy()
+        res[name] = {"rel_o": float(np.linalg.norm(og - o_ref) / np.linalg.norm(o_ref)),
+                     "maxrel_o": float(np.max(np.abs(og - o_ref)) / np.max(np.abs(o_ref))),
+                     "rel_ht": float(np.linalg.norm(ht.double().numpy() - ht_ref) / np.linalg.norm(ht_ref))}
+    return res
+
+
 def run_gb300(args):
     import torch
     rank, world, local = rank_info()
@@ -301,24 +472,23 @@ def run_gb300(args):
     if st != 0:
         raise RuntimeError(f"kernel status {st}")
 
-    # timed region: K full forwards back to back
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    # timed region: K full forwards back to back, an event between consecutive steps
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks.mark_start()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-    ev[1].record(stream)
-    torch.cuda.synchronize(dev)
+    per_step, span_ms = time_steps(step, args.steps, stream)
     clocks.mark_end()
     barrier(world)
+    med = statistics.median(per_step)
+    # clock-only window: untimed back-to-back steps right after the region
+    window_steps = clock_window(step, med, clocks)
     clk = clocks.stop()
-    total_ms = ev[0].elapsed_time(ev[1])
-    ms_per_step = max_over_ranks(total_ms / args.steps, world)
+    clk["clock_window_steps"] = window_steps
+    ms_per_step = max_over_ranks(med, world)
+    ms_mean = max_over_ranks(span_ms / args.steps, world)
 
     # per-kernel split (separate steps with an event between the two kernels)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -340,19 +510,25 @@ def run_gb300(args):
     b_intra, b_scan = bytes_per_token_head(K, V)
     th = tokens * H
     hstate = 2 * N * H * K * V * 4 if x["h0"] is not None else N * H * K * V * 4
-    intra_avg = statistics.mean(intra_ms)
-    scan_avg = statistics.mean(scan_ms)
-    if scan_avg >= intra_avg:
-        dom, dom_ms, dom_bytes, src = "kda_scan_kernel", scan_avg, b_scan * th + hstate, "scan.cu"
+    intra_med = statistics.median(intra_ms)
+    scan_med = statistics.median(scan_ms)
+    if scan_med >= intra_med:
+        dom, dom_ms, dom_bytes, src = "kda_scan_kernel", scan_med, b_scan * th + hstate, "scan.cu"
     else:
-        dom, dom_ms, dom_bytes, src = "kda_intra_kernel", intra_avg, b_intra * th, "intra.cu"
+        dom, dom_ms, dom_bytes, src = "kda_intra_kernel", intra_med, b_intra * th, "intra.cu"
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = ncu_traffic(dom, os.path.join(ROOT, "chunked_gated_delta_gb300", "csrc", src), w.name)
-    step_bytes = (b_intra + b_scan) * th + hstate
-    step_flops = flops_per_token_head(K, V) * th
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     e2e = run_e2e(args, kda, x, dims, stream, dev, world) if args.e2e_steps > 0 else None
+    small = gpu_parity_small(kda, dev) if (rank == 0 and not args.no_cpu_baseline) else None
+    del ws, o, ht, d
+    torch.cuda.empty_cache()
+    others = {}
+    if args.configs and rank == 0:
+        for name in ("mid", "varlen", "long"):
+            if name != args.workload:
+                others[name] = measure_workload(kda, name, dev, min(args.steps, 50), hbm, tc)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -360,26 +536,33 @@ def run_gb300(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the KDA forward workloads)",
         "config": workload_config(w, x),
+        "timing": {"ms_per_step_median": ms_per_step, "ms_p10": pct(per_step, 0.1), "ms_p90": pct(per_step, 0.9),
+                   "ms_per_step_mean": ms_mean, "per_step_events": True,
+                   "note": "value = tokens / median per-step time (CUDA events between consecutive steps on the "
+                           "launching stream, max over ranks)"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms},
-        "step_roofline": {"bytes": step_bytes, "hbm_ms": step_bytes / (hbm * 1e9) * 1e3,
-                          "flops": step_flops, "tc_ms": step_flops / (tc * 1e12) * 1e3,
-                          "frac_of_hbm_bound": (step_bytes / (hbm * 1e9) * 1e3) / ms_per_step},
-        "kernels_ms": {"intra": intra_avg, "scan": scan_avg, "note": "separate split steps with an event "
-                       "between the kernels over every chunk; the timed steps run them back to back"
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                     "launch_ms_statistic": "median over the split steps"},
+        "step_roofline": step_roofline(K, V, th, hstate, ms_per_step, hbm, tc),
+        "kernels_ms": {"intra": intra_med, "scan": scan_med, "note": "medians of separate split steps with an "
+                       "event between the kernels over every chunk; the timed steps run them back to back"
                        + (f", in {lay.stage_count} chunk ranges of {lay.stage_len} chunks (each range's "
                           "intra kernel beside the previous range's scan)" if lay.stage_count > 1 else "")},
+        "plan": plan_name(lay),
         "e2e": e2e,
         # planner + intra + scan (+ map pass and combine when the scan is segmented;
         # planner + one intra and one scan per chunk range when the forward is staged)
         "gpu_launches": launches_per_step(lay) * args.steps,
         "clocks": clk,
     }
+    if others:
+        line["other_workloads"] = others
     if rank == 0 and not args.no_cpu_baseline:
         r, desc, thr, _ = oracle_sample_rate(x, args.ref_seconds, host_cores())
         line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": desc}
+        line["parity"] = parity_figures(small)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -464,30 +647,27 @@ def run_gb300_bwd(args):
     torch.cuda.synchronize(dev)
     if kda.status(ws, stream) != 0:
         raise RuntimeError("kernel status")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks.mark_start()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
+    per, span_ms = time_steps(step, args.steps, stream)
     clocks.mark_end()
     barrier(world)
+    med = statistics.median(per)
+    window_steps = clock_window(step, med, clocks)
     clk = clocks.stop()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    ms_per_step = max_over_ranks(ev[0].elapsed_time(ev[-1]) / args.steps, world)
+    clk["clock_window_steps"] = window_steps
+    ms_per_step = max_over_ranks(med, world)
     tokens = B * T if x["cu_seqlens"] is None else int(x["cu_seqlens"][-1])
     value = tokens * world / (ms_per_step / 1e3)
     hbm, _, _, peak_kind = peaks()
     th = tokens * H
     state = N * H * K * V * 4 * (2 if gr["dht"] is not None else 1)
     by = bwd_bytes_per_token_head(K, V) * th + state
-    avg = statistics.mean(per)
+    avg = med
     achieved = by / (avg / 1e3) / 1e9
     traffic = ncu_traffic("kda_bwd_dh_kernel", os.path.join(ROOT, "chunked_gated_delta_gb300", "csrc",
                                                             "bwd_dh.cu"), w.name)
@@ -531,6 +711,8 @@ def run_gb300_bwd(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; forward workload inputs plus N(0,1) upstream gradients)",
         "config": {**workload_config(w, x), "path": "bwd_dh"},
+        "timing": {"ms_per_step_median": ms_per_step, "ms_p10": pct(per, 0.1), "ms_p90": pct(per, 0.9),
+                   "ms_per_step_mean": span_ms / args.steps, "per_step_events": True},
         "roofline": {"bound": "hbm", "kernel": "kda_bwd_dh_kernel", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": by, "avg_launch_ms": avg},
@@ -602,6 +784,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=2.0,
                     help="target wall seconds of one bounded oracle sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the extra per-workload lines (mid, varlen, long) of the forward")
     ap.add_argument("--path", choices=("fwd", "bwd_dh"), default="fwd",
                     help="fwd: the forward (default); bwd_dh: the reverse state scan")
     args = ap.parse_args()

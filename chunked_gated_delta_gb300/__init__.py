@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     KdaError,
     bwd_dh,
     chunk_table,
+    exact_path_tiles,
     fwd,
     fwd_host,
     fwd_intra,

@@ -247,6 +247,16 @@ def status(workspace, stream=None) -> int:
     return int(load_library().kda_fwd_status(_ptr(workspace), _stream_handle(stream)))
 
 
+def exact_path_tiles(workspace, dims: Dims, stream=None) -> int:
+    """Synchronise the stream and return the diagnostic count of (chunk, head)
+    tiles whose gated sums took the exact per-element path in the last
+    forward on this workspace (the int32 after the status word)."""
+    import torch
+    status(workspace, stream)
+    off = workspace_layout(dims).status + 4
+    return int(workspace[off:off + 4].cpu().view(torch.int32).item())
+
+
 def host_arena_size(dims: Dims) -> int:
     return int(load_library().kda_fwd_host_arena_size(ctypes.byref(dims)))
 

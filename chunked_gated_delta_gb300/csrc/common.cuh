@@ -23,6 +23,10 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Status word bits (workspace, int32).
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadSeqlens = 2;
+// Index of the int32 after the status word that counts the (chunk, head)
+// tiles of the last forward whose gated sums took the exact per-element path
+// (a diagnostic; the planner resets it with the status word).
+constexpr int kStatusExactTiles = 1;
 
 struct SeqInfo {
     int32_t bos, len, tile_base, tiles;

@@ -75,6 +75,11 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 // memory beyond their own need, so no intra-chunk CTA shares an SM with them.
 cudaError_t launch_scan_stage(const ScanArgs& a, int stage, cudaStream_t stream);
 cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream);
+// Argument checks of the scan stage of kda_fwd (h0, o, ht, dims, workspace),
+// with no driver call and no launch: lets an entry point that runs the two
+// stages itself report every argument error before it enqueues anything.
+kda_status check_scan_args(const void* h0, void* o, void* ht, const kda_dims* dims, void* workspace,
+                           size_t workspace_bytes);
 // h_in[j+1] = P_j h_in[j] + Q_j over the segment maps in L.pq (h_in[0] = h0)
 cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, int N, int H, int K, int V,
                                int flags, cudaStream_t stream);

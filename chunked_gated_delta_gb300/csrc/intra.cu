@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
     if (warp == 0 && !mbar_wait(&bar_qk, 0, kWaitLimitNs)) timed_out = true;
     const bool exact_path = __syncthreads_or(unsafe) != 0;
+    if (exact_path && tid == 0) atomicAdd(status + kStatusExactTiles, 1);  // diagnostic count
 
     uint16_t* aqk_g = reinterpret_cast<uint16_t*>(ws + L.aqk) + tile * 64 * 64;
 

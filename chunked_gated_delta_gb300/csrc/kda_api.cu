@@ -85,7 +85,10 @@ __global__ void __launch_bounds__(kPlanThreads)
         }
         chunks[c] = ci;
     }
-    if (tid == 0) status[0] = ok ? 0 : kStatusBadSeqlens;
+    if (tid == 0) {
+        status[0] = ok ? 0 : kStatusBadSeqlens;
+        status[kStatusExactTiles] = 0;
+    }
 }
 
 // ---------------------------------------------------------------- validation
@@ -411,6 +414,15 @@ kda_status run_stages(const IntraArgs& ia, const ScanArgs& sa, cudaStream_t s) {
     return ok && joined ? KDA_OK : KDA_ERR_CUDA;
 }
 }  // namespace
+
+}  // extern "C"
+
+kda_status kda::check_scan_args(const void* h0, void* o, void* ht, const kda_dims* dims, void* workspace,
+                                size_t workspace_bytes) {
+    return scan_check(h0, o, ht, dims, nullptr, workspace, workspace_bytes);
+}
+
+extern "C" {
 
 kda_status kda_fwd_intra_ex(const void* q, const void* k, const void* v, const float* g,
                             const void* beta, const int32_t* cu_seqlens, const kda_dims* dims,

@@ -4,7 +4,7 @@
 #include <mutex>
 
 #include "../../include/kda.h"
-#include "common.cuh"
+#include "internal.h"
 
 namespace {
 
@@ -53,9 +53,13 @@ extern "C" kda_status kda_fwd_noalloc(const void* q, const void* k, const void* 
     kda_status err = KDA_OK;
     void* scratch = scratch_on_current_device(&err);
     if (!scratch) return err;
-    // the two stages in order on the caller's stream (kda_fwd may instead run a
-    // long single sequence in chunk ranges on two streams that the library
-    // creates; this entry point creates nothing)
+    // every argument of the scan stage is checked before the intra stage
+    // enqueues anything (the intra stage checks its own before it launches)
+    err = kda::check_scan_args(h0, o, ht, dims, scratch, kScratchBytes);
+    if (err != KDA_OK) return err;
+    // the two stages in order on the caller's stream, which is kda_fwd's own
+    // plan for every problem that fits the scratch (kda_fwd runs chunk ranges
+    // on library streams only for workspaces of hundreds of MB)
     kda_status st = kda_fwd_intra(q, k, v, g, beta, cu_seqlens, dims, scratch, kScratchBytes, stream);
     if (st != KDA_OK) return st;
     return kda_fwd_scan(scale, h0, o, ht, dims, scratch, kScratchBytes, stream);

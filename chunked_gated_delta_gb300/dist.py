@@ -7,9 +7,15 @@ Two ways to use N GPUs:
 * replicas (weak scaling, what ``bench.py --gpus N`` measures): every rank
   runs its own batch of the workload; the job's throughput is the tokens of
   all ranks over the slowest rank's time;
-* sharding one batch (strong scaling): :func:`shard_range` gives each rank a
-  contiguous block of sequences (or of heads); each rank writes a disjoint
-  slice of o and ht.
+* sharding one batch (strong scaling): :func:`plan_shard` gives each rank a
+  contiguous block of sequences (or, with fewer sequences than ranks, of
+  heads), :func:`take_shard` cuts the rank's block out of the batch as a
+  problem of its own (a batch slice for fixed length; for a packed batch the
+  rows of its sequences with ``cu_seqlens`` rebased to start at 0, and the
+  matching rows of ``h0``), :func:`fwd_shard` runs the forward on it, and
+  :func:`place_shard` writes the block's o and ht into the full tensors.
+  Each rank's o and ht are disjoint slices of the whole, so nothing is
+  exchanged on the data path.
 
 Only the timing needs communication: a barrier around the timed region and a
 max over ranks of the elapsed time (:func:`max_over_ranks`), which works on
@@ -57,3 +63,83 @@ def barrier(world: int) -> None:
 def job_throughput(units_per_rank, max_seconds: float) -> float:
     """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
     return float(sum(units_per_rank)) / max_seconds
+
+
+class Shard:
+    """One rank's block of a batch: sequences [s0, s1) and heads [h0, h1), with
+    the packed token rows [r0, r1) of those sequences (packed batches) or the
+    batch rows [s0, s1) (fixed length)."""
+
+    __slots__ = ("s0", "s1", "h0", "h1", "r0", "r1", "varlen")
+
+    def __init__(self, s0, s1, h0, h1, r0, r1, varlen):
+        self.s0, self.s1, self.h0, self.h1, self.r0, self.r1, self.varlen = s0, s1, h0, h1, r0, r1, varlen
+
+    def __repr__(self):
+        return (f"Shard(seqs=[{self.s0},{self.s1}), heads=[{self.h0},{self.h1}), rows=[{self.r0},{self.r1}), "
+                f"varlen={self.varlen})")
+
+
+def plan_shard(B: int, T: int, H: int, rank: int, world: int, cu_seqlens=None) -> Shard:
+    """This rank's block.  Sequences are split into contiguous blocks (each
+    rank's inputs and outputs are then contiguous slices); with fewer
+    sequences than ranks the heads are split instead.  ``cu_seqlens`` is the
+    packed batch's offsets as host integers (a list, or a CPU tensor), or
+    None for B fixed-length sequences of T tokens."""
+    varlen = cu_seqlens is not None
+    cu = [int(c) for c in cu_seqlens] if varlen else None
+    N = len(cu) - 1 if varlen else B
+    if N >= world:
+        s0, s1 = shard_range(N, rank, world)
+        hb, he = 0, H
+    else:
+        s0, s1 = 0, N
+        hb, he = shard_range(H, rank, world)
+    r0, r1 = (cu[s0], cu[s1]) if varlen else (s0, s1)
+    return Shard(s0, s1, hb, he, r0, r1, varlen)
+
+
+def take_shard(sh: Shard, q, k, v, g, beta, h0=None, cu_seqlens=None):
+    """The block's inputs as a problem of its own: (q, k, v, g, beta, h0,
+    cu_seqlens).  A block of whole sequences is a slice (no copy, except the
+    rebased cu_seqlens); a block of heads is a strided slice and is copied
+    into contiguous tensors."""
+    if sh.varlen:
+        rows = slice(sh.r0, sh.r1)
+        q, k, v, g, beta = (t[:, rows] for t in (q, k, v, g, beta))
+        cu = cu_seqlens[sh.s0:sh.s1 + 1] - cu_seqlens[sh.s0]
+    else:
+        b = slice(sh.s0, sh.s1)
+        q, k, v, g, beta = (t[b] for t in (q, k, v, g, beta))
+        cu = None
+    if h0 is not None:
+        h0 = h0[sh.s0:sh.s1]
+    if (sh.h0, sh.h1) != (0, v.shape[2]):
+        hs = slice(sh.h0, sh.h1)
+        q, k, v, g = (t[:, :, hs].contiguous() for t in (q, k, v, g))
+        beta = beta[:, :, hs].contiguous()
+        if h0 is not None:
+            h0 = h0[:, hs].contiguous()
+    return q, k, v, g, beta, h0, cu
+
+
+def fwd_shard(sh: Shard, q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_state=True,
+              stream=None):
+    """The forward (the library's kda_fwd through the binding) on this rank's
+    block; returns the block's (o, ht)."""
+    from . import binding
+    lq, lk, lv, lg, lb, lh0, lcu = take_shard(sh, q, k, v, g, beta, h0, cu_seqlens)
+    return binding.fwd(lq, lk, lv, lg, lb, scale, h0=lh0, cu_seqlens=lcu, output_final_state=output_final_state,
+                       stream=stream)
+
+
+def place_shard(sh: Shard, o_local, ht_local, o, ht=None):
+    """Writes a block's (o, ht) into the full outputs (any device; a copy)."""
+    rows = slice(sh.r0, sh.r1)
+    hs = slice(sh.h0, sh.h1)
+    if sh.varlen:
+        o[:, rows, hs] = o_local
+    else:
+        o[rows, :, hs] = o_local
+    if ht is not None and ht_local is not None:
+        ht[sh.s0:sh.s1, hs] = ht_local

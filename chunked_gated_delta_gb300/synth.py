@@ -164,8 +164,9 @@ def make_variant_inputs(w: Workload, io_dtype=torch.bfloat16, qk_heads=None, bet
 
 
 def make_inputs_on(w: Workload, device, with_bwd: bool = False):
-    """Inputs of the fixed-length workload ``w`` drawn directly on ``device``
-    with a generator seeded there (the distributions of :func:`make_inputs`).
+    """Inputs of the workload ``w`` drawn directly on ``device`` with a
+    generator seeded there (the distributions of :func:`make_inputs`; a packed
+    workload takes the seeded lengths of :func:`make_inputs`).
 
     For problems whose tensors are too large to draw on the CPU in a test's
     time: the bits differ from :func:`make_inputs` (another generator), so a
@@ -173,10 +174,14 @@ def make_inputs_on(w: Workload, device, with_bwd: bool = False):
     device.  ``with_bwd`` adds do, dv_in (N(0,1) bf16) and dht (N(0, 0.1^2)
     fp32), as :func:`make_bwd_inputs` draws them.
     """
-    if w.varlen:
-        raise ValueError("make_inputs_on draws fixed-length workloads only")
     gen = torch.Generator(device=device).manual_seed(w.seed)
-    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    H, K, V = w.H, w.K, w.V
+    cu = None
+    if w.varlen:  # the seeded lengths of make_inputs, packed as one row of sequences
+        cu = cu_from_lengths(varlen_lengths(w.varlen, w.max_len, w.seed + 7919))
+        B, T, N = 1, int(cu[-1]), w.varlen
+    else:
+        B, T, N = w.B, w.T, w.B
 
     def randn(shape):
         return torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
@@ -193,10 +198,10 @@ def make_inputs_on(w: Workload, device, with_bwd: bool = False):
     g = randn((B, T, H, K))
     g += w.mu
     g = F.logsigmoid(g)
-    h0 = 0.1 * randn((B, H, K, V)) if w.h0 else None
-    out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=None, scale=K ** -0.5,
-               B=B, T=T, H=H, K=K, V=V, N=B)
+    h0 = 0.1 * randn((N, H, K, V)) if w.h0 else None
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=None if cu is None else cu.to(device),
+               scale=K ** -0.5, B=B, T=T, H=H, K=K, V=V, N=N)
     if with_bwd:
         out.update(do=randn((B, T, H, V)).to(torch.bfloat16), dv_in=randn((B, T, H, V)).to(torch.bfloat16),
-                   dht=0.1 * randn((B, H, K, V)))
+                   dht=0.1 * randn((N, H, K, V)))
     return out

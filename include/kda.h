@@ -239,9 +239,11 @@ kda_status kda_fwd_host(const void* q, const void* k, const void* v, const float
                         void* stream);
 
 /*
- * Scratch capacity of kda_fwd_noalloc: 64 MiB, enough for the workspace of
- * about 56 thousand token-heads at K = V = 128 (e.g. T = 1792 tokens with
- * H = 32, or T = 57344 with H = 1).
+ * Scratch capacity of kda_fwd_noalloc: 64 MiB.  A problem fits when
+ * kda_fwd_workspace_size(dims) is at most this size: at K = V = 128 that is
+ * T <= 1792 tokens with H = 32, or T <= 53248 with H = 1 (a long single
+ * sequence adds the segment maps of the segmented scan to the workspace, so
+ * the token-head capacity is lower there than for many heads).
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -315,6 +317,11 @@ int32_t kda_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int32_t chu
  * Byte offsets of the regions inside the workspace, for inspection of the
  * intra-chunk intermediates (tests).  `max_chunks` is the chunk capacity
  * the layout was sized for.  Returns KDA_ERR_INVALID_ARG for invalid dims.
+ * The status region holds the status word (int32 at `status`) and, in the
+ * int32 after it, a diagnostic count of the (chunk, head) tiles of the last
+ * forward whose gated sums took the exact per-element path (chunks whose
+ * log2 decay span exceeds 96, where the factored gate products would
+ * overflow); the planner resets both.
  */
 typedef struct kda_ws_layout {
     size_t status, seq_info, chunk_info, gd, qg, kg, w, u, aqk, total;

@@ -276,3 +276,25 @@ def test_workspace_regions_hold_what_the_kernels_write():
         if L.stage_count > 1:
             assert N == 1 and (L.stage_count - 1) * L.stage_len < (T + 63) // 64 <= L.stage_count * L.stage_len
         assert kda.workspace_size(d) == L.total
+
+
+def test_noalloc_capacity_and_plan():
+    """kda_fwd_noalloc runs the two stages on the caller's stream; kda_fwd would
+    run a staged plan (library streams) only for problems whose workspace far
+    exceeds the scratch array, so within the scratch capacity both entry
+    points take the same plan.  Also pins the capacity the header states."""
+    cap = kda.binding.NOALLOC_SCRATCH_BYTES
+
+    def fits(B, T, H, K, V, n=0):
+        s = kda.workspace_size(kda.make_dims(B, T, H, K, V, n))
+        return 0 < s <= cap
+
+    assert fits(1, 53248, 1, 128, 128) and not fits(1, 53249, 1, 128, 128)
+    assert fits(1, 1792, 32, 128, 128) and not fits(1, 1793, 32, 128, 128)
+    for H in (1, 2, 3, 8, 16, 24, 32, 48, 64, 128):
+        for K, V in ((128, 128), (64, 64), (128, 64), (64, 128)):
+            for T in list(range(1, 110000, 1777)) + [53248, 101376]:
+                for d in (kda.make_dims(1, T, H, K, V), kda.make_dims(1, T, H, K, V, 1)):
+                    s = kda.workspace_size(d)
+                    if 0 < s <= cap:
+                        assert kda.workspace_layout(d).stage_count == 1, (T, H, K, V)

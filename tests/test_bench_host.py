@@ -80,3 +80,23 @@ def test_host_arena_of_time_slices(dims):
     per = -(-nt // 8)
     slice_ws = kda.workspace_size(kda.make_dims(B, per * 64, H, K, V))
     assert arena >= slice_ws
+
+
+def test_short_region_reports_the_clock_window():
+    """A timed region shorter than the sampling period holds no sample; the
+    clock-only window of untimed steps after it supplies the figure, labelled."""
+    samples = [(0.0, _line(800)), (0.31, _line(2070)), (0.36, _line(2055)), (0.41, _line(2070)), (1.5, _line(900))]
+    c = _sampler(samples, 0.10, 0.113)
+    c.mark_window(0.3, 0.45)
+    rec = c.stop()
+    assert rec["samples_in_region"] == 0 and rec["samples_clock_window"] == 3
+    assert rec["window"].startswith("clock window") and rec["samples"] == 3 and rec["sm_mhz"] == 2070.0
+
+
+def test_percentiles_and_strict_roofline():
+    assert bench.pct([4.0, 1.0, 3.0, 2.0], 0.5) == 2.5 and bench.pct([1.0], 0.9) == 1.0
+    assert bench.pct(list(range(11)), 0.1) == 1.0 and bench.pct(list(range(11)), 0.9) == 9.0
+    assert bench.strict_bytes_per_token_head(128, 128) == 1538
+    r = bench.step_roofline(128, 128, 1000, 0, 1.0, 1000.0, 1000.0)
+    assert r["bytes"] == 3858 * 1000 and r["strict_io_bytes"] == 1538 * 1000
+    assert abs(r["frac_of_strict_io_bound"] - 1538e3 / 1e12 * 1e3) < 1e-12

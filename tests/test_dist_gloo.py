@@ -1,7 +1,12 @@
-"""Multi-rank host logic on CPU (gloo, world_size 2): sharding of (sequence,
-head) units across ranks needs no exchange on the data path; only the timing
-is reduced (max over ranks).  Each rank runs the oracle on its shard in place
-of the GPU kernel, and the shards must reassemble to the single-rank result."""
+"""Multi-rank host logic on CPU (gloo, world_size 2): a batch is sharded into
+contiguous blocks of (sequence, head) units, one per rank, with no exchange on
+the data path; only the timing is reduced (max over ranks).  Each rank cuts
+its block out of the batch with the same helpers the GPU path uses
+(dist.plan_shard / take_shard: a batch slice, or a packed block with
+cu_seqlens rebased to 0 and the matching h0 rows, or a block of heads), runs
+the oracle on it as a problem of its own in place of the GPU kernel, and the
+blocks, placed back with dist.place_shard, must reassemble to the single-rank
+result bit for bit."""
 import os
 import socket
 
@@ -20,14 +25,18 @@ def _free_port():
     return port
 
 
-def _lengths():
-    return [37, 0, 64, 130, 5]
+CASES = {
+    "packed": dict(lengths=[37, 0, 64, 130, 5], B=1, T=0, H=3),   # sequence blocks, rebased offsets
+    "fixed": dict(lengths=None, B=3, T=70, H=3),                 # batch slices
+    "heads": dict(lengths=None, B=1, T=90, H=5),                  # one sequence: blocks of heads
+}
 
 
-def _inputs():
+def _inputs(case):
     from chunked_gated_delta_gb300 import synth
-    w = synth.Workload("dist", B=1, T=0, H=3, K=16, V=8, seed=123)
-    return synth.make_inputs(w, lengths=_lengths())
+    c = CASES[case]
+    w = synth.Workload("dist", B=c["B"], T=c["T"], H=c["H"], K=16, V=8, seed=123)
+    return synth.make_inputs(w, lengths=c["lengths"])
 
 
 def _worker(rank, world, port, out_dir):
@@ -40,14 +49,17 @@ def _worker(rank, world, port, out_dir):
     try:
         r, w, lr = kdist.rank_info()
         assert (r, w, lr) == (rank, world, rank)
-        x = _inputs()
-        s0, s1 = kdist.shard_range(x["N"], r, w)
-        units = [(s, h) for s in range(s0, s1) for h in range(x["H"])]
-        o, ht = oracle.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
-                                     cu_seqlens=x["cu_seqlens"], units=units)
-        np.save(os.path.join(out_dir, f"o{rank}.npy"), o)
-        np.save(os.path.join(out_dir, f"ht{rank}.npy"), ht)
-        np.save(os.path.join(out_dir, f"range{rank}.npy"), np.array([s0, s1]))
+        for case in CASES:
+            x = _inputs(case)
+            cu = None if x["cu_seqlens"] is None else x["cu_seqlens"].tolist()
+            sh = kdist.plan_shard(x["B"], x["T"], x["H"], r, w, cu)
+            q, k, v, g, beta, h0, lcu = kdist.take_shard(sh, x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                                         x["h0"], x["cu_seqlens"])
+            if lcu is not None:
+                assert int(lcu[0]) == 0 and int(lcu[-1]) == q.shape[1]
+            o, ht = oracle.recurrent_fwd(q, k, v, g, beta, x["scale"], h0=h0, cu_seqlens=lcu)
+            np.save(os.path.join(out_dir, f"{case}_o{rank}.npy"), o)
+            np.save(os.path.join(out_dir, f"{case}_ht{rank}.npy"), ht)
         assert kdist.max_over_ranks(float(rank + 1), w) == float(world)
         kdist.barrier(w)
     finally:
@@ -67,21 +79,33 @@ def test_shard_range_tiles_exactly():
     assert kdist.job_throughput([100, 300], 2.0) == 200.0
 
 
+def test_plan_shard_covers_every_unit_once():
+    for B, T, H, cu in [(4, 100, 3, None), (1, 100, 8, None), (1, 0, 4, [0, 5, 5, 9, 20, 20, 31])]:
+        for world in (1, 2, 3, 5):
+            seen = []
+            for r in range(world):
+                sh = kdist.plan_shard(B, T, H, r, world, cu)
+                seen += [(s, h) for s in range(sh.s0, sh.s1) for h in range(sh.h0, sh.h1)]
+                if cu is not None:
+                    assert (sh.r0, sh.r1) == (cu[sh.s0], cu[sh.s1])
+            N = B if cu is None else len(cu) - 1
+            assert sorted(seen) == [(s, h) for s in range(N) for h in range(H)], (B, H, cu, world)
+
+
 def test_two_rank_gloo_sharding(tmp_path):
     import oracle
     world = 2
     mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
-    x = _inputs()
-    o_full, ht_full = oracle.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
-                                           h0=x["h0"], cu_seqlens=x["cu_seqlens"])
-    cu = x["cu_seqlens"].tolist()
-    covered = []
-    for r in range(world):
-        s0, s1 = np.load(tmp_path / f"range{r}.npy")
-        o = np.load(tmp_path / f"o{r}.npy")
-        ht = np.load(tmp_path / f"ht{r}.npy")
-        for s in range(s0, s1):
-            covered.append(s)
-            np.testing.assert_array_equal(o[:, cu[s]:cu[s + 1]], o_full[:, cu[s]:cu[s + 1]])
-            np.testing.assert_array_equal(ht[s], ht_full[s])
-    assert sorted(covered) == list(range(x["N"]))
+    for case in CASES:
+        x = _inputs(case)
+        o_full, ht_full = oracle.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
+                                               h0=x["h0"], cu_seqlens=x["cu_seqlens"])
+        o = np.full_like(o_full, np.nan)
+        ht = np.full_like(ht_full, np.nan)
+        cu = None if x["cu_seqlens"] is None else x["cu_seqlens"].tolist()
+        for r in range(world):
+            sh = kdist.plan_shard(x["B"], x["T"], x["H"], r, world, cu)
+            kdist.place_shard(sh, np.load(tmp_path / f"{case}_o{r}.npy"), np.load(tmp_path / f"{case}_ht{r}.npy"),
+                              o, ht)
+        np.testing.assert_array_equal(o, o_full)
+        np.testing.assert_array_equal(ht, ht_full)

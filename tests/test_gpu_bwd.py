@@ -14,7 +14,7 @@ import torch
 
 from chunked_gated_delta_gb300 import synth
 from oracle import chunked as oc
-from parity_util import make, sample_units, to_dev
+from parity_util import UNIT_MIN_TOKENS, UNIT_REL, _Acc, make, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -110,6 +110,8 @@ def assert_bwd_within(res, what=""):
             assert val <= REL, (what, res)
         elif key.startswith("maxrel_"):
             assert val <= MAXREL, (what, res)
+        elif key.startswith("unit_"):
+            assert val <= UNIT_REL, (what, res)
         else:
             assert val <= 1e-6, (what, res)
 
@@ -175,20 +177,52 @@ def test_mid_workload_full():
     full_bwd_check(x, synth.make_bwd_inputs(x), "mid")
 
 
-# ------------------------------------------------------------------ full sizes, sampled
+# ------------------------------------------------------------------ full sizes, every element
 
-def _sampled(name, n, include=()):
+def pooled_bwd_check(x, gr, gpu, what):
+    """Every unit of a full-size workload against the fp64 oracle, run in a
+    spawn process pool (tests/bwd_pool.py) and compared unit by unit as the
+    results arrive (pooled norms plus each unit's own relative error)."""
+    import bwd_pool
+    dhck_g, dv2_g, dh0_g = gpu
+    H, V = x["H"], x["V"]
+    rows = x["B"] * x["T"]
+    xn = {n: x[n].float().numpy().reshape((rows, H) + tuple(x[n].shape[3:])) for n in ("q", "k", "v", "g", "beta")}
+    gn = {"do": gr["do"].float().numpy().reshape(rows, H, V), "dv_in": gr["dv_in"].float().numpy().reshape(rows, H, V),
+          "dht": None if gr["dht"] is None else gr["dht"].float().numpy()}
+    starts, lens, base = _bounds(x)
+    dv2_n = dv2_g.float().cpu().numpy().reshape(rows, H, V)
+    dhck_c = dhck_g.cpu()
+    dh0_n = dh0_g.float().cpu().numpy()
+    acc = {"dv2": _Acc(), "dhck": _Acc(), "dh0": _Acc()}
+    units = [(s, h) for s in range(x["N"]) for h in range(H)]
+    for (s, h), ck, d2, d0 in bwd_pool.map_units(bwd_pool.unit_jobs(xn, gn, x["scale"], units, starts, lens)):
+        full = lens[s] >= UNIT_MIN_TOKENS
+        acc["dv2"].add(dv2_n[starts[s]:starts[s] + lens[s], h], d2, (s, h), full)
+        acc["dhck"].add(dhck_c[int(base[s]):int(base[s + 1]), h].double().numpy(), ck, (s, h), full)
+        acc["dh0"].add(dh0_n[s, h], d0, (s, h), full)
+    res = {}
+    for name, a in acc.items():
+        assert a.finite, f"non-finite values in {name}"
+        if a.n and a.sr > 0:
+            res[f"rel_{name}"] = a.rel()
+            res[f"maxrel_{name}"] = a.maxrel()
+            res[f"unit_{name}"] = a.worst
+    print(f"[parity] bwd {what}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()), flush=True)
+    assert_bwd_within(res, what)
+    return res
+
+
+def _full(name):
     x = synth.make_inputs(synth.WORKLOADS[name])
     gr = synth.make_bwd_inputs(x)
-    units = sample_units(x, n, seed=3, include=include)
     gpu = run_bwd(x, gr)
-    res = compare_bwd(x, gpu, oracle_bwd(x, gr, units=units), units=units)
-    assert_bwd_within(res, name)
+    pooled_bwd_check(x, gr, gpu, name)
     return x, gr, gpu
 
 
-def test_headline_workload_sampled_and_linear():
-    x, gr, (dhck, dv2, dh0) = _sampled("headline", 4, include=[(0, 0), (3, 31)])
+def test_headline_workload_full_and_linear():
+    x, gr, (dhck, dv2, dh0) = _full("headline")
     # the reverse scan is linear in (do, dv_in, dht): doubling them doubles every
     # output bit for bit (power-of-two scaling commutes with every rounding)
     gr2 = {k_: 2 * v_ for k_, v_ in gr.items()}
@@ -198,12 +232,12 @@ def test_headline_workload_sampled_and_linear():
     assert torch.equal(dh02, 2 * dh0)
 
 
-def test_varlen_workload_sampled():
-    _sampled("varlen", 6)
+def test_varlen_workload_full():
+    _full("varlen")
 
 
-def test_long_workload_sampled():
-    _sampled("long", 2, include=[(0, 0)])
+def test_long_workload_full():
+    _full("long")
 
 
 def test_deterministic():
@@ -247,14 +281,11 @@ def test_segmented_no_dht():
     full_bwd_check(x, synth.make_bwd_inputs(x, dht=False), "segmented, dht None")
 
 
-def test_long_k64_workload_sampled():
+def test_long_k64_workload_full():
     x = synth.make_inputs(synth.WORKLOADS["long_k64"])
     assert _seg_plan(x).seg_count >= 2
     gr = synth.make_bwd_inputs(x)
-    units = sample_units(x, 2, seed=4, include=[(0, 0)])
-    gpu = run_bwd(x, gr)
-    res = compare_bwd(x, gpu, oracle_bwd(x, gr, units=units), units=units)
-    assert_bwd_within(res, "long_k64")
+    pooled_bwd_check(x, gr, run_bwd(x, gr), "long_k64")
 
 
 def test_grouped_value_heads():

@@ -3,9 +3,11 @@
 latency-critical path where cudaMalloc would synchronise the device).  Its
 workspace is the library's built-in scratch array.
 
-The test calls it through the C ABI twice in a row, on different problems, and
-checks each result against kda_fwd with a caller-allocated workspace, within
-the tolerances of the parity tests.  This file is collected last on purpose.
+The test calls it through the C ABI on several problems in a row (two small
+ones, then one long single sequence near the scratch capacity that takes the
+segmented scan) and checks each result against kda_fwd with a
+caller-allocated workspace and against the fp64 oracle, within the
+tolerances of the parity tests.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -13,7 +15,7 @@ import torch
 
 import chunked_gated_delta_gb300 as kda
 from chunked_gated_delta_gb300 import synth
-from parity_util import MAXREL_O, REL_HT, REL_O, make, to_dev
+from parity_util import MAXREL_O, REL_HT, REL_O, assert_within, compare, make, oracle_ref, to_dev
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -38,15 +40,22 @@ def _both(x):
     return o, ht, o_ref, ht_ref
 
 
-def test_noalloc_matches_kda_fwd_on_two_calls_in_a_row():
+def test_noalloc_matches_kda_fwd_and_the_oracle_on_calls_in_a_row():
     first = synth.make_inputs(make(B=2, T=300, H=4, seed=71))
     second = synth.make_inputs(make(T=0, H=3, seed=72), lengths=[65, 1, 200, 64])
-    for x in (first, second):
-        o, ht, o_ref, ht_ref = _both(x)
-        rel, maxrel = _rel(o, o_ref)
+    # near the capacity at H = 1 (T <= 53248): one sequence whose scan is segmented
+    third = synth.make_inputs(make(B=1, T=50000, H=1, seed=73))
+    dims = kda.make_dims(1, 50000, 1, 128, 128)
+    assert kda.workspace_layout(dims).seg_count > 1
+    assert kda.workspace_size(dims) <= kda.binding.NOALLOC_SCRATCH_BYTES
+    for x in (first, second, third):
+        o, ht, o_dev, ht_dev = _both(x)
+        rel, maxrel = _rel(o, o_dev)
         assert rel <= REL_O and maxrel <= MAXREL_O, (rel, maxrel)
-        rel_h, _ = _rel(ht, ht_ref)
+        rel_h, _ = _rel(ht, ht_dev)
         assert rel_h <= REL_HT, rel_h
+        o_ref, ht_ref = oracle_ref(x)
+        assert_within(compare(x, o, ht, o_ref, ht_ref), "noalloc against the oracle")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
