@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     FwdOpts,
     KdaError,
     bwd_dh,
+    chain_states,
     chunk_table,
     exact_path_tiles,
     fwd,
@@ -24,6 +25,7 @@ from .binding import (  # noqa: F401
     make_dims,
     new_workspace,
     selftest_wait_timeout,
+    state_map,
     status,
     status_string,
     workspace_layout,

@@ -25,7 +25,8 @@ STATUS_NAMES = {
 EXPORTS = ("kda_fwd_workspace_size", "kda_fwd", "kda_fwd_intra", "kda_fwd_scan", "kda_fwd_status",
            "kda_status_string", "kda_chunk_table", "kda_workspace_layout", "kda_fwd_host_arena_size",
            "kda_fwd_host", "kda_fwd_noalloc", "kda_selftest_wait_timeout", "kda_bwd_dh",
-           "kda_fwd_ex", "kda_fwd_intra_ex", "kda_fwd_scan_ex", "kda_bwd_dh_ex")
+           "kda_fwd_ex", "kda_fwd_intra_ex", "kda_fwd_scan_ex", "kda_bwd_dh_ex", "kda_fwd_state_map",
+           "kda_chain_states")
 
 
 class KdaError(RuntimeError):
@@ -96,6 +97,8 @@ def load_library(build_if_missing: bool = True):
             "kda_fwd_intra_ex": (ctypes.c_int, [P, P, P, P, P, P, D, O, P, SZ, P]),
             "kda_fwd_scan_ex": (ctypes.c_int, [F32, P, P, P, D, O, P, SZ, P]),
             "kda_bwd_dh_ex": (ctypes.c_int, [F32, P, P, P, P, P, P, D, O, P, SZ, P]),
+            "kda_fwd_state_map": (ctypes.c_int, [P, P, P, P, P, P, P, D, P, SZ, P]),
+            "kda_chain_states": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -240,6 +243,43 @@ def fwd_scan(scale, h0, o, ht, dims: Dims, workspace, stream=None):
     rc = load_library().kda_fwd_scan(float(scale), _ptr(h0), _ptr(o), _ptr(ht), ctypes.byref(dims),
                                      _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "kda_fwd_scan")
+
+
+def state_map(q, k, v, g, beta, cu_seqlens=None, workspace=None, stream=None):
+    """kda_fwd_state_map: the affine state map [P | Q] (fp32 [N, H, K, K + V])
+    of these tokens of every (sequence, head).  Returns (pq, workspace, dims);
+    the workspace keeps the intra-chunk intermediates for fwd_scan."""
+    import torch
+    _check_inputs(q, k, v, g, beta, None, cu_seqlens)
+    if q.dtype != torch.bfloat16 or q.shape[2] != v.shape[2]:
+        raise TypeError("state_map takes the default interface (bf16 I/O, equal heads)")
+    dims, N = _dims_of(q, v, cu_seqlens)
+    K, V, H = q.shape[-1], v.shape[-1], v.shape[2]
+    if workspace is None:
+        workspace = new_workspace(dims, q.device)
+    pq = torch.empty((N, H, K, K + V), dtype=torch.float32, device=q.device)
+    rc = load_library().kda_fwd_state_map(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(pq),
+                                          ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                          _stream_handle(stream))
+    _check(rc, "kda_fwd_state_map")
+    return pq, workspace, dims
+
+
+def chain_states(pq_all, h0=None, stream=None):
+    """kda_chain_states: entry states h_in [R, N, H, K, V] of R consecutive token
+    ranges from their gathered maps pq_all [R, N, H, K, K + V] (fp32, CUDA)."""
+    import torch
+    if pq_all.dtype != torch.float32 or not pq_all.is_cuda or not pq_all.is_contiguous() or pq_all.dim() != 5:
+        raise TypeError("pq_all must be a contiguous CUDA float32 tensor [R, N, H, K, K + V]")
+    R, N, H, K, KV = pq_all.shape
+    V = KV - K
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_cuda or not h0.is_contiguous()
+                           or tuple(h0.shape) != (N, H, K, V)):
+        raise TypeError("h0 must be a contiguous CUDA float32 tensor [N, H, K, V]")
+    h_in = torch.empty((R, N, H, K, V), dtype=torch.float32, device=pq_all.device)
+    rc = load_library().kda_chain_states(_ptr(pq_all), _ptr(h0), _ptr(h_in), R, N, H, K, V, _stream_handle(stream))
+    _check(rc, "kda_chain_states")
+    return h_in
 
 
 def status(workspace, stream=None) -> int:

@@ -32,6 +32,8 @@ constexpr int kScanModeOutput = 0;  // the scan with its output o (and ht)
 constexpr int kScanModeMap = 1;     // per-segment affine maps [P | Q] (segmented scan)
 constexpr int kScanExitToHin = 4;   // output mode: a segment that ends before its sequence
                                     // stores its exit state as the next one's entry (hin)
+constexpr int kScanMapOut = 8;      // map mode over each whole sequence: [P | Q] to ScanArgs::ht
+                                    // as fp32 [N, H, K, K + V] (the affine map of the tokens given)
 
 struct ScanArgs {
     CUtensorMap tm_w, tm_qg, tm_kg, tm_u, tm_aqk;  // workspace tiles, 2-D {dim, tiles*64}
@@ -83,5 +85,12 @@ kda_status check_scan_args(const void* h0, void* o, void* ht, const kda_dims* di
 // h_in[j+1] = P_j h_in[j] + Q_j over the segment maps in L.pq (h_in[0] = h0)
 cudaError_t launch_seg_combine(const void* h0, uint8_t* ws, const WsLayout& L, int N, int H, int K, int V,
                                int flags, cudaStream_t stream);
+// The affine map [P | Q] of every (sequence, head) over all of its chunks, from
+// the intermediates in a.ws, stored to a.ht as fp32 [N, H, K, K + V].
+cudaError_t launch_scan_map_out(const ScanArgs& a, cudaStream_t stream);
+// h_in[0] = h0 (fp32, or zeros if null) and h_in[r+1] = P_r h_in[r] + Q_r for
+// r < ranges - 1 over pq fp32 [ranges, N, H, K, K + V]; h_in fp32 [ranges, N, H, K, V].
+cudaError_t launch_chain_states(const float* pq, const float* h0, float* h_in, int ranges, int N, int H, int K,
+                                int V, cudaStream_t stream);
 
 }  // namespace kda

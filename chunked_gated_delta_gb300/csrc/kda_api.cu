@@ -299,9 +299,11 @@ kda_status scan_check(const void* h0, void* o, void* ht, const kda_dims* dims, c
 }
 
 // Validation and TMA descriptors of the scan stage.  Launches nothing.
+// with_o = false: the map pass of kda_fwd_state_map (no o, no tensor map of it).
 kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_dims* dims,
-                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, ScanArgs* a) {
-    kda_status st = scan_check(h0, o, ht, dims, opts, workspace, workspace_bytes);
+                      const kda_fwd_opts* opts, void* workspace, size_t workspace_bytes, ScanArgs* a,
+                      bool with_o = true) {
+    kda_status st = with_o ? scan_check(h0, o, ht, dims, opts, workspace, workspace_bytes) : KDA_OK;
     if (st != KDA_OK) return st;
     kda_fwd_opts op{};
     if (opts) op = *opts;
@@ -317,7 +319,7 @@ kda_status scan_setup(float scale, const void* h0, void* o, void* ht, const kda_
         ok = ok && map2(&a->tm_kg, ws + L.kg, dims->K, trows);
         ok = ok && map2(&a->tm_u, ws + L.u, dims->V, trows);
         ok = ok && map2(&a->tm_aqk, ws + L.aqk, kChunk, trows);
-        if (rows > 0) {  // o [rows, H, V]: a box is 32 token rows of one head's 64 columns
+        if (rows > 0 && with_o) {  // o [rows, H, V]: a box is 32 token rows of one head's 64 columns
             const uint64_t odims[3] = {(uint64_t)dims->V, (uint64_t)dims->H, (uint64_t)rows};
             const uint64_t ostr[2] = {(uint64_t)dims->V * 2, (uint64_t)dims->V * 2 * dims->H};
             const uint32_t obox[3] = {64, 1, 32};
@@ -535,6 +537,43 @@ kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* 
     if (run && ia.L.stage_count > 1) return run_stages(ia, sa, s);
     if (run && launch_intra(ia, s) != cudaSuccess) return KDA_ERR_CUDA;
     return launch_scan(sa, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_fwd_state_map(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                             const int32_t* cu_seqlens, float* pq, const kda_dims* dims, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    // every argument is checked before any driver call or launch
+    if (!dims) return KDA_ERR_INVALID_ARG;
+    kda_status st = check_dims(dims, is_varlen(dims));
+    if (st != KDA_OK) return st;
+    const int64_t N = is_varlen(dims) ? dims->num_seqs : dims->B;
+    if (N * dims->H > 0 && !pq) return KDA_ERR_INVALID_ARG;
+    if (pq && !aligned(pq, 16)) return KDA_ERR_ALIGNMENT;
+    IntraArgs ia;
+    bool run = false;
+    st = intra_setup(q, k, v, g, beta, dims->H, 0, cu_seqlens, dims, nullptr, workspace, workspace_bytes, &ia, &run);
+    if (st != KDA_OK) return st;
+    ScanArgs sa;
+    st = scan_setup(1.0f, nullptr, nullptr, pq, dims, nullptr, workspace, workspace_bytes, &sa, false);
+    if (st != KDA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = plan(cu_seqlens, dims, ia, s);
+    if (st != KDA_OK) return st;
+    if (run && launch_intra(ia, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return launch_scan_map_out(sa, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_chain_states(const float* pq, const float* h0, float* h_in, int32_t ranges, int32_t num_seqs,
+                            int32_t H, int32_t K, int32_t V, void* stream) {
+    if (ranges < 1 || num_seqs < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+    if ((K != 64 && K != 128) || (V != 64 && V != 128)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!pq || !h_in) return KDA_ERR_INVALID_ARG;
+    if (!aligned(pq, 16) || !aligned(h_in, 16) || (h0 && !aligned(h0, 16))) return KDA_ERR_ALIGNMENT;
+    return launch_chain_states(pq, h0, h_in, ranges, num_seqs, H, K, V, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
 }
 
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,

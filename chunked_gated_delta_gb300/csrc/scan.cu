@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
     // this CTA's chunks [c_begin, c_end) of the sequence
     const int c_begin = seg * L.seg_len;
     const int c_end = min(tiles, c_begin + L.seg_len);
+    const bool map_out = (flags & kScanMapOut) != 0;  // map of the whole sequence, to the caller
     if (seg > 0 && c_begin >= tiles) return;   // the sequence has fewer segments
-    if (map_mode && c_end >= tiles) return;    // the last segment's map is never used
+    if (map_mode && !map_out && c_end >= tiles) return;  // the last segment's map is never used
     const int nit = c_end > c_begin ? c_end - c_begin : 0;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -325,8 +326,8 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             write_h();
         }
         if (map_mode && has_row && !timed_out && !*abort_flag) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(ws + L.pq) +
-                                                    ((((int64_t)seg * N + s) * H + h) * K + r) * (K + V) + col);
+            float* base = map_out ? static_cast<float*>(ht) : reinterpret_cast<float*>(ws + L.pq);
+            float4* dst = reinterpret_cast<float4*>(base + ((((int64_t)seg * N + s) * H + h) * K + r) * (K + V) + col);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 dst[j] = make_float4(hreg[4 * j], hreg[4 * j + 1], hreg[4 * j + 2], hreg[4 * j + 3]);
@@ -540,7 +541,9 @@ cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream, int 
     if (e != cudaSuccess) return e;
     const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
     const int64_t ctas = (int64_t)a.N * a.H * (ncol / S::BV);
-    const int segs = stage >= 0 ? 1 : mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const int segs = (stage >= 0 || (a.flags & kScanMapOut)) ? 1
+                     : mode == kScanModeMap                 ? a.L.seg_count - 1
+                                                            : a.L.seg_count;
     if (ctas <= 0 || segs <= 0) return cudaSuccess;
     WsLayout L = a.L;
     int flags = a.flags;
@@ -558,7 +561,9 @@ cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream, int 
 template <int KB>
 cudaError_t launch_scan_k(const ScanArgs& a, int mode, cudaStream_t stream, int sms, int stage = -1) {
     const int ncol = mode == kScanModeMap ? a.K + a.V : a.V;
-    const int segs = stage >= 0 ? 1 : mode == kScanModeMap ? a.L.seg_count - 1 : a.L.seg_count;
+    const int segs = (stage >= 0 || (a.flags & kScanMapOut)) ? 1
+                     : mode == kScanModeMap                 ? a.L.seg_count - 1
+                                                            : a.L.seg_count;
     const ScanShape sh = scan_shape((int64_t)a.N * a.H * (ncol / 64) * segs, ncol, sms);
     // Few CTAs: each SM holds at most one, so give it a two-deep input ring.
     if (sh.nvb == 1 && sh.stages == 2) return launch_scan_t<KB, 1, 2>(a, mode, stream, stage);
@@ -590,9 +595,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// The same kernel chains the maps of consecutive token ranges for the
+// context-parallel forward: explicit pointers, a fixed count of maps
+// (nseg_fixed > 0, no sequence table, no status word) and h_in[0] = h0
+// written out too.
 template <int K>
-__global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __restrict__ h0, uint8_t* __restrict__ ws,
-                                                                const WsLayout L, const int N, const int H,
+__global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __restrict__ h0,
+                                                                const float* __restrict__ pq,
+                                                                float* __restrict__ hin,
+                                                                const int32_t* __restrict__ status,
+                                                                const SeqInfo* __restrict__ seqs, const int seg_len,
+                                                                const int nseg_fixed, const int N, const int H,
                                                                 const int V, const int flags) {
     constexpr int C = kCombineCols, K4 = K / 4, HK4 = K4 / 2, NTH = 2 * K;
     extern __shared__ float4 csm4[];
@@ -600,16 +613,24 @@ __global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __re
     float4* Hs = csm4 + 2 * K * K4;  // 2 x [K][C / 4]
     const int NTV = V / C;
     const int vt = blockIdx.x % NTV, h = (blockIdx.x / NTV) % H, s = blockIdx.x / (NTV * H);
-    const int32_t* status = reinterpret_cast<const int32_t*>(ws + L.status);
-    if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
-    const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
-    const int nseg = (si.tiles + L.seg_len - 1) / L.seg_len;
-    if (nseg < 2) return;
+    if (status != nullptr && *reinterpret_cast<const volatile int32_t*>(status) != 0) return;
+    int nseg = nseg_fixed;
+    if (nseg_fixed <= 0) {
+        const SeqInfo si = seqs[s];
+        nseg = (si.tiles + seg_len - 1) / seg_len;
+    }
     const int tid = threadIdx.x;
     const int col0 = vt * C;
     const int r = tid >> 1, half = tid & 1;  // state row, half of the key dims
-    const float* pq = reinterpret_cast<const float*>(ws + L.pq);
-    float* hin = reinterpret_cast<float*>(ws + L.hin);
+    if (nseg_fixed > 0 && half == 0) {  // h_in[0] = h0 (the first range's entry)
+        float4* dst = reinterpret_cast<float4*>(hin + (((int64_t)s * H + h) * K + r) * V + col0);
+        const float* src = h0 != nullptr ? static_cast<const float*>(h0) + (((int64_t)s * H + h) * K + r) * V + col0
+                                         : nullptr;
+#pragma unroll
+        for (int c4 = 0; c4 < C / 4; ++c4)
+            dst[c4] = src != nullptr ? *reinterpret_cast<const float4*>(src + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (nseg < 2) return;
     auto map_of = [&](int j) { return pq + (((int64_t)j * N + s) * H + h) * K * (K + V); };
     auto stage_p = [&](int j) {  // issue the copies of P_j into buffer j & 1
         const float* PQ = map_of(j);
@@ -694,15 +715,26 @@ __global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __re
 }
 
 template <int K>
-cudaError_t launch_combine_k(const ScanArgs& a, cudaStream_t stream) {
+cudaError_t launch_combine_raw(const void* h0, const float* pq, float* hin, const int32_t* status,
+                               const SeqInfo* seqs, int seg_len, int nseg_fixed, int N, int H, int V, int flags,
+                               cudaStream_t stream) {
     const uint32_t smem = (2 * K * (K / 4) + 2 * K * (kCombineCols / 4)) * sizeof(float4);
     auto kern = kda_seg_combine_kernel<K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int64_t ctas = (int64_t)a.N * a.H * (a.V / kCombineCols);
+    const int64_t ctas = (int64_t)N * H * (V / kCombineCols);
     if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, 2 * K, smem, stream>>>(a.h0, a.ws, a.L, a.N, a.H, a.V, a.flags);
+    kern<<<(unsigned)ctas, 2 * K, smem, stream>>>(h0, pq, hin, status, seqs, seg_len, nseg_fixed, N, H, V, flags);
     return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_combine_k(const ScanArgs& a, cudaStream_t stream) {
+    return launch_combine_raw<K>(a.h0, reinterpret_cast<const float*>(a.ws + a.L.pq),
+                                 reinterpret_cast<float*>(a.ws + a.L.hin),
+                                 reinterpret_cast<const int32_t*>(a.ws + a.L.status),
+                                 reinterpret_cast<const SeqInfo*>(a.ws + a.L.seq_info), a.L.seg_len, 0, a.N, a.H,
+                                 a.V, a.flags, stream);
 }
 
 }  // namespace
@@ -738,6 +770,23 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     return run(kScanModeOutput);
+}
+
+cudaError_t launch_scan_map_out(const ScanArgs& a, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    if (a.K != 128 && a.K != 64) return cudaErrorInvalidValue;
+    ScanArgs m = a;
+    m.flags |= kScanMapOut;
+    m.L.seg_len = 0x7fffffff;  // one segment: every chunk of each sequence
+    return a.K == 128 ? launch_scan_k<2>(m, kScanModeMap, stream, sms) : launch_scan_k<1>(m, kScanModeMap, stream, sms);
+}
+
+cudaError_t launch_chain_states(const float* pq, const float* h0, float* h_in, int ranges, int N, int H, int K, int V,
+                                cudaStream_t stream) {
+    if (ranges < 1) return cudaErrorInvalidValue;
+    if (K == 128) return launch_combine_raw<128>(h0, pq, h_in, nullptr, nullptr, 1, ranges, N, H, V, 0, stream);
+    if (K == 64) return launch_combine_raw<64>(h0, pq, h_in, nullptr, nullptr, 1, ranges, N, H, V, 0, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_scan_stage(const ScanArgs& a, int stage, cudaStream_t stream) {

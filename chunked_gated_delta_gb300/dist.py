@@ -17,9 +17,19 @@ Two ways to use N GPUs:
   Each rank's o and ht are disjoint slices of the whole, so nothing is
   exchanged on the data path.
 
-Only the timing needs communication: a barrier around the timed region and a
-max over ranks of the elapsed time (:func:`max_over_ranks`), which works on
-both the gloo (CPU) and NCCL backends.
+* one sequence split along T (context parallel), the one layout that needs
+  an exchange: :func:`plan_time_shard` gives each rank a contiguous token
+  range (on 64-token chunk boundaries); each rank computes its range's affine
+  state map [P | Q] (``kda_fwd_state_map``), the maps are all-gathered in rank
+  order (K x (K + V) fp32 per sequence and head), ``kda_chain_states``
+  composes them into every range's entry state, and each rank finishes its
+  range with the scan from its entry state (:func:`fwd_context_parallel`, or
+  :func:`context_parallel_maps` / :func:`context_parallel_finish` around an
+  exchange of the caller's own).
+
+Only the timing needs communication otherwise: a barrier around the timed
+region and a max over ranks of the elapsed time (:func:`max_over_ranks`),
+which works on both the gloo (CPU) and NCCL backends.
 """
 from __future__ import annotations
 
@@ -143,3 +153,61 @@ def place_shard(sh: Shard, o_local, ht_local, o, ht=None):
         o[rows, :, hs] = o_local
     if ht is not None and ht_local is not None:
         ht[sh.s0:sh.s1, hs] = ht_local
+
+
+# ---------------------------------------------------------------- context parallel
+
+CHUNK = 64
+
+
+def plan_time_shard(T: int, rank: int, world: int):
+    """This rank's token range [t0, t1) of sequences of T tokens split along T
+    across `world` ranks: contiguous, in rank order, on 64-token chunk
+    boundaries (every rank's chunks are then chunks of the whole sequence),
+    the chunk counts differing by at most one."""
+    nt = (T + CHUNK - 1) // CHUNK
+    c0, c1 = shard_range(nt, rank, world)
+    return min(T, c0 * CHUNK), min(T, c1 * CHUNK)
+
+
+def context_parallel_maps(q, k, v, g, beta, cu_seqlens=None, stream=None):
+    """Pass 1 on this rank's tokens: the affine map [P | Q] of its range for
+    every (sequence, head), fp32 [N, H, K, K + V].  Returns (pq, workspace,
+    dims); keep the workspace for :func:`context_parallel_finish`."""
+    from . import binding
+    return binding.state_map(q, k, v, g, beta, cu_seqlens=cu_seqlens, stream=stream)
+
+
+def context_parallel_finish(pq_all, rank: int, workspace, dims, scale, h0=None, output_final_state=True,
+                            stream=None):
+    """After the exchange: pq_all [R, N, H, K, K + V] holds every range's map in
+    rank order.  Chains them into the entry states, then runs this rank's scan
+    from its entry state on the workspace of pass 1.  Returns (o, ht): this
+    rank's outputs [B, T_r, H, V] and the state after its range (on the last
+    rank, the sequences' final state)."""
+    import torch
+    from . import binding
+    h_in = binding.chain_states(pq_all, h0, stream=stream)
+    R, N, H, K, KV = pq_all.shape
+    V = KV - K
+    o = torch.empty((dims.B, dims.T, H, V), dtype=torch.bfloat16, device=pq_all.device)
+    ht = torch.empty((N, H, K, V), dtype=torch.float32, device=pq_all.device) if output_final_state else None
+    binding.fwd_scan(scale, h_in[rank], o, ht, dims, workspace, stream)
+    return o, ht
+
+
+def fwd_context_parallel(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, group=None, stream=None):
+    """The forward of sequences split along T across the ranks of `group`
+    (torch.distributed, one GPU per rank): q, k, v, g, beta (and cu_seqlens)
+    hold this rank's tokens of every sequence, the ranks' ranges in rank
+    order; h0 is the sequences' initial state (every rank passes the same).
+    One all-gather of the maps is the only exchange.  Returns this rank's
+    (o, ht) as :func:`context_parallel_finish`."""
+    import torch
+    import torch.distributed as tdist
+    rank, world = tdist.get_rank(group), tdist.get_world_size(group)
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    pq, ws, dims = context_parallel_maps(q, k, v, g, beta, cu_seqlens, stream)
+    parts = [torch.empty_like(pq) for _ in range(world)]
+    tdist.all_gather(parts, pq, group=group)
+    return context_parallel_finish(torch.stack(parts), rank, ws, dims, scale, h0, stream=stream)

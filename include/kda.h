@@ -280,6 +280,48 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const fl
                            void* stream);
 
 /*
+ * Context-parallel forward (sequences split along T across ranks), the pass
+ * before the exchange.  The state after a run of tokens is an affine function
+ * of the state before it: with the chunked update h <- exp2(G) * h + kg^T v',
+ * v' = u - w h, of kernel-fun "kda/_kernels/fwd_state.py" (module docstring),
+ * each chunk maps h to M_c h + kg^T u with M_c = Diag(exp2 G) - kg^T w, so a
+ * range of chunks maps h_in to
+ *     h_out = P h_in + Q,   P = the product of its M_c,  Q = h_out from h_in = 0.
+ * For every sequence s and head h of the local problem (this rank's tokens of
+ * each sequence; same dims, q, k, v, g, beta and cu_seqlens conventions as
+ * kda_fwd), this call runs the intra-chunk stage and a scan over the K + V
+ * columns [P | Q], started from [I | 0], and stores
+ *   pq        fp32 [N, H, K, K + V]   P in columns 0..K-1, Q in K..K+V-1
+ *             (device, 16-byte aligned; N = num_seqs or B).
+ * An empty sequence gives P = I, Q = 0.  The intra-chunk intermediates stay
+ * in `workspace` (>= kda_fwd_workspace_size(dims) bytes), so that after the
+ * exchange kda_fwd_scan(scale, h_in, o, ht, dims, workspace, ...) on the same
+ * workspace produces this rank's o and its exit state from the entry state
+ * h_in (kda_chain_states).  P and Q are computed with the same bf16 operand
+ * copies as the scan itself, so the composed result matches a single call to
+ * the forward's tolerances (not bit for bit).  Asynchronous on `stream`;
+ * kernel-side errors via kda_fwd_status(workspace).
+ */
+kda_status kda_fwd_state_map(const void* q, const void* k, const void* v, const float* g,
+                             const void* beta, const int32_t* cu_seqlens, float* pq,
+                             const kda_dims* dims, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Context-parallel forward, after the exchange: the entry state of each of
+ * `ranges` consecutive token ranges, from their maps gathered in rank order,
+ *     h_in[0] = h0,   h_in[r + 1] = P_r h_in[r] + Q_r   (fp32),
+ *   pq    fp32 [ranges, num_seqs, H, K, K + V]  (kda_fwd_state_map of range r at pq[r])
+ *   h0    fp32 [num_seqs, H, K, V] or NULL = zeros
+ *   h_in  fp32 [ranges, num_seqs, H, K, V] out (the last range's map is not needed)
+ * All device pointers, 16-byte aligned.  K, V in {64, 128}.  Asynchronous on
+ * `stream`; returns KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_ALIGNMENT
+ * before any launch.
+ */
+kda_status kda_chain_states(const float* pq, const float* h0, float* h_in, int32_t ranges,
+                            int32_t num_seqs, int32_t H, int32_t K, int32_t V, void* stream);
+
+/*
  * Synchronises `stream` and returns the error the kernels recorded in
  * `workspace` during the last kda_fwd / kda_fwd_intra / kda_fwd_scan on it
  * (KDA_OK, KDA_ERR_BAD_SEQLENS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the

@@ -298,3 +298,30 @@ def test_noalloc_capacity_and_plan():
                     s = kda.workspace_size(d)
                     if 0 < s <= cap:
                         assert kda.workspace_layout(d).stage_count == 1, (T, H, K, V)
+
+
+def test_context_parallel_entries_validate_before_any_launch(lib):
+    """kda_fwd_state_map and kda_chain_states reject bad arguments before any
+    driver call (on this machine a launch would fail with KDA_ERR_CUDA)."""
+    P = ctypes.c_void_p
+    d = kda.make_dims(2, 130, 2, 128, 128)
+
+    def smap(dims=d, q=FAKE, pq=FAKE, ws=FAKE, ws_bytes=1 << 40):
+        return lib.kda_fwd_state_map(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(pq),
+                                     ctypes.byref(dims) if dims is not None else None, P(ws), ws_bytes, None)
+
+    assert smap(dims=None) == 1                                       # NULL dims
+    assert smap(dims=kda.make_dims(2, 130, 2, 96, 128)) == 2          # K unsupported
+    assert smap(pq=0) == 1                                            # no output
+    assert smap(pq=FAKE + 8) == 3                                     # misaligned output
+    assert smap(q=FAKE + 2) == 3                                      # misaligned q
+    assert smap(ws_bytes=1024) == 4                                   # workspace too small
+
+    def chain(pq=FAKE, h0=None, h_in=FAKE, R=2, N=2, H=2, K=128, V=128):
+        return lib.kda_chain_states(P(pq), P(h0), P(h_in), R, N, H, K, V, None)
+
+    assert chain(R=0) == 1 and chain(N=-1) == 1 and chain(H=0) == 1   # counts
+    assert chain(K=96) == 2 and chain(V=32) == 2                      # unsupported dims
+    assert chain(pq=0) == 1 and chain(h_in=0) == 1                    # NULL pointers
+    assert chain(pq=FAKE + 4) == 3 and chain(h0=FAKE + 4) == 3        # misaligned
+    assert chain(N=0) == 0                                            # nothing to do

@@ -109,3 +109,86 @@ def test_two_rank_gloo_sharding(tmp_path):
                               o, ht)
         np.testing.assert_array_equal(o, o_full)
         np.testing.assert_array_equal(ht, ht_full)
+
+
+# ------------------------------------------------------------------ context parallel (T split)
+
+def _cp_inputs():
+    from chunked_gated_delta_gb300 import synth
+    w = synth.Workload("cp", B=2, T=300, H=2, K=16, V=8, seed=321)
+    return synth.make_inputs(w)
+
+
+def _oracle_map(q, k, v, g, beta, scale):
+    """[P | Q] of a token range by the oracle: P from h0 = I with v = 0 (the
+    state map alone), Q from h0 = 0; fp64 [B, H, K, K + V]."""
+    import torch
+
+    import oracle
+    B, T, H, K = q.shape
+    eye = torch.eye(K, dtype=torch.float32).expand(B, H, K, K).contiguous()
+    v0 = torch.zeros((B, T, H, K), dtype=torch.bfloat16)
+    _, P = oracle.recurrent_fwd(q, k, v0, g, beta, scale, h0=eye)
+    _, Q = oracle.recurrent_fwd(q, k, v, g, beta, scale, h0=None)
+    return np.concatenate([P, Q], axis=-1)
+
+
+def _cp_worker(rank, world, port, out_dir):
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        x = _cp_inputs()
+        t0, t1 = kdist.plan_time_shard(x["T"], rank, world)
+        loc = {n: x[n][:, t0:t1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+        pq = torch.from_numpy(_oracle_map(loc["q"], loc["k"], loc["v"], loc["g"], loc["beta"], x["scale"]))
+        parts = [torch.empty_like(pq) for _ in range(world)]
+        dist.all_gather(parts, pq)  # the one exchange, in rank order
+        K = x["K"]
+        h = x["h0"].double().numpy()
+        for r in range(rank):  # the chain: h_in[r + 1] = P_r h_in[r] + Q_r
+            P, Q = parts[r].numpy()[..., :K], parts[r].numpy()[..., K:]
+            h = np.einsum("bhij,bhjv->bhiv", P, h) + Q
+        f64 = {n: loc[n].double() for n in loc}  # the exact input values; the entry state stays fp64
+        o, ht = oracle.recurrent_fwd(f64["q"], f64["k"], f64["v"], f64["g"], f64["beta"], x["scale"],
+                                     h0=h, fp64_inputs=True)
+        np.save(os.path.join(out_dir, f"cp_o{rank}.npy"), o)
+        np.save(os.path.join(out_dir, f"cp_ht{rank}.npy"), ht)
+        np.save(os.path.join(out_dir, f"cp_hin{rank}.npy"), h)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_plan_time_shard_covers_the_sequence():
+    for T in (0, 1, 63, 64, 65, 300, 4097):
+        for world in (1, 2, 3, 8):
+            spans = [kdist.plan_time_shard(T, r, world) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == T
+            assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+            assert all(a[0] % 64 == 0 or a[0] == T for a in spans)  # chunk boundaries (or an empty tail)
+
+
+def test_two_rank_gloo_context_parallel(tmp_path):
+    """Two gloo ranks split two sequences of 300 tokens along T: each maps its
+    range ([P | Q] by the oracle), the maps are all-gathered, each chains them
+    into its entry state and runs its range from there.  The concatenated
+    outputs and the last rank's final state equal the unsplit oracle to fp64
+    rounding (the composition only reassociates the same products)."""
+    import oracle
+    world = 2
+    mp.spawn(_cp_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    x = _cp_inputs()
+    o_full, ht_full = oracle.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"])
+    o = np.concatenate([np.load(tmp_path / f"cp_o{r}.npy") for r in range(world)], axis=1)
+    ht = np.load(tmp_path / f"cp_ht{world - 1}.npy")
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)  # noqa: E731
+    assert rel(o, o_full) < 1e-10 and rel(ht, ht_full) < 1e-10
+    # rank 1's entry state is the state after rank 0's tokens
+    t0, t1 = kdist.plan_time_shard(x["T"], 0, world)
+    _, h_mid = oracle.recurrent_fwd(*(x[n][:, t0:t1].contiguous() for n in ("q", "k", "v", "g", "beta")),
+                                    x["scale"], h0=x["h0"])
+    assert rel(np.load(tmp_path / "cp_hin1.npy"), h_mid) < 1e-10
