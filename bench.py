@@ -454,9 +454,14 @@ def run_gb300(args):
               P(d["cu_seqlens"]), P(o), P(ht), ctypes.byref(dims), P(ws), ctypes.c_size_t(ws.numel()),
               ctypes.c_void_p(stream.cuda_stream))
 
+    fused = args.plan == "fused"
+    opts = kda.FwdOpts(0, 0, 0, 0, kda.binding.PLAN_FUSED if fused else kda.binding.PLAN_AUTO)
+    args_ex = args_c[:10] + (ctypes.byref(dims), ctypes.byref(opts)) + args_c[11:]
+
     def step():
-        # one full forward through the C ABI (planner, intra-chunk kernel, scan)
-        rc = lib.kda_fwd(*args_c)
+        # one full forward through the C ABI (planner, intra-chunk kernel, scan;
+        # or planner and the single-pass fused kernel)
+        rc = lib.kda_fwd_ex(*args_ex) if fused else lib.kda_fwd(*args_c)
         if rc != 0:
             raise RuntimeError(kda.status_string(rc))
 
@@ -501,6 +506,9 @@ def run_gb300(args):
     torch.cuda.synchronize(dev)
     intra_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
     scan_ms = [ev1[i].elapsed_time(ev0[i + 1]) for i in range(args.steps)]
+    if fused:  # restore the fused path's outputs (the split steps overwrote o / ht)
+        step()
+        torch.cuda.synchronize(dev)
     tokens = B * T
     value = tokens * world / (ms_per_step / 1e3)
 
@@ -512,7 +520,10 @@ def run_gb300(args):
     hstate = 2 * N * H * K * V * 4 if x["h0"] is not None else N * H * K * V * 4
     intra_med = statistics.median(intra_ms)
     scan_med = statistics.median(scan_ms)
-    if scan_med >= intra_med:
+    if fused:  # one kernel moving the strict single-pass I/O (the planner is microseconds)
+        dom, dom_ms, dom_bytes, src = ("kda_fused_kernel", ms_per_step,
+                                       strict_bytes_per_token_head(K, V) * th + hstate, "fused.cu")
+    elif scan_med >= intra_med:
         dom, dom_ms, dom_bytes, src = "kda_scan_kernel", scan_med, b_scan * th + hstate, "scan.cu"
     else:
         dom, dom_ms, dom_bytes, src = "kda_intra_kernel", intra_med, b_intra * th, "intra.cu"
@@ -520,7 +531,7 @@ def run_gb300(args):
     traffic = ncu_traffic(dom, os.path.join(ROOT, "chunked_gated_delta_gb300", "csrc", src), w.name)
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, kda, x, dims, stream, dev, world) if args.e2e_steps > 0 else None
+    e2e = run_e2e(args, kda, x, dims, stream, dev, world) if (args.e2e_steps > 0 and not fused) else None
     small = gpu_parity_small(kda, dev) if (rank == 0 and not args.no_cpu_baseline) else None
     del ws, o, ht, d
     torch.cuda.empty_cache()
@@ -549,11 +560,12 @@ def run_gb300(args):
                        "event between the kernels over every chunk; the timed steps run them back to back"
                        + (f", in {lay.stage_count} chunk ranges of {lay.stage_len} chunks (each range's "
                           "intra kernel beside the previous range's scan)" if lay.stage_count > 1 else "")},
-        "plan": plan_name(lay),
+        "plan": "single-pass fused kernel (one CTA per sequence and head)" if fused else plan_name(lay),
         "e2e": e2e,
         # planner + intra + scan (+ map pass and combine when the scan is segmented;
-        # planner + one intra and one scan per chunk range when the forward is staged)
-        "gpu_launches": launches_per_step(lay) * args.steps,
+        # planner + one intra and one scan per chunk range when the forward is staged;
+        # planner + the fused kernel on the fused plan)
+        "gpu_launches": (2 if fused else launches_per_step(lay)) * args.steps,
         "clocks": clk,
     }
     if others:
@@ -786,6 +798,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the extra per-workload lines (mid, varlen, long) of the forward")
+    ap.add_argument("--plan", choices=("auto", "fused"), default="auto",
+                    help="auto: the two-stage forward (default); fused: the single-pass kernel "
+                         "(KDA_PLAN_FUSED), timed against the strict single-pass I/O bound")
     ap.add_argument("--path", choices=("fwd", "bwd_dh"), default="fwd",
                     help="fwd: the forward (default); bwd_dh: the reverse state scan")
     args = ap.parse_args()

@@ -44,11 +44,13 @@ class Dims(ctypes.Structure):
 class FwdOpts(ctypes.Structure):
     """kda_fwd_opts: interface variants of the forward (all zero = kda_fwd)."""
     _fields_ = [("io_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
-                ("beta_logits", ctypes.c_int32), ("qk_heads", ctypes.c_int32)]
+                ("beta_logits", ctypes.c_int32), ("qk_heads", ctypes.c_int32), ("plan", ctypes.c_int32)]
 
 
 IO_BF16, IO_F16 = 0, 1
 STATE_F32, STATE_BF16 = 0, 1
+PLAN_AUTO, PLAN_TWO_STAGE, PLAN_FUSED = 0, 1, 2
+PLANS = {None: PLAN_AUTO, "auto": PLAN_AUTO, "two_stage": PLAN_TWO_STAGE, "fused": PLAN_FUSED}
 
 
 class WsLayout(ctypes.Structure):
@@ -191,7 +193,8 @@ def new_workspace(dims: Dims, device):
 
 
 def fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_state=True,
-        workspace=None, out=None, final_state=None, stream=None, beta_logits=False, state_dtype=None):
+        workspace=None, out=None, final_state=None, stream=None, beta_logits=False, state_dtype=None,
+        plan=None):
     """KDA chunked forward on the GPU.  Returns (o, ht) (ht None if not requested).
 
     q, k: [B,T,Hqk,K]; v: [B,T,H,V]; beta: [B,T,H], all bf16 or all fp16 (o
@@ -201,7 +204,10 @@ def fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_sta
     head h // (H // Hqk)).  ``beta_logits``: beta holds logits, the kernel
     applies the sigmoid.  ``state_dtype`` (torch.float32 / torch.bfloat16) of ht;
     defaults to h0's dtype, else fp32.  ``workspace`` (uint8 CUDA tensor) may be
-    passed to avoid an allocation per call.
+    passed to avoid an allocation per call.  ``plan``: None / "auto" /
+    "two_stage" (the two kernels; the workspace keeps the intermediates for
+    bwd_dh) or "fused" (the single-pass kernel: bf16 I/O, fp32 state, activated
+    beta, equal heads).
     """
     import torch
     _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
@@ -215,9 +221,11 @@ def fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_final_sta
         state_dtype = h0.dtype if h0 is not None else torch.float32
     if h0 is not None and h0.dtype != state_dtype:
         raise TypeError("h0 and ht must have the same dtype")
+    if plan not in PLANS:
+        raise ValueError(f"plan must be one of {sorted(k for k in PLANS if k)}")
     opts = FwdOpts(IO_F16 if q.dtype == torch.float16 else IO_BF16,
                    STATE_BF16 if state_dtype == torch.bfloat16 else STATE_F32,
-                   1 if beta_logits else 0, Hqk if Hqk != H else 0)
+                   1 if beta_logits else 0, Hqk if Hqk != H else 0, PLANS[plan])
     if workspace is None:
         workspace = new_workspace(dims, q.device)
     o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)

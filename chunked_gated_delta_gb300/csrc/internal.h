@@ -67,6 +67,19 @@ struct BwdArgs {
 constexpr int kBwdF16 = 1;         // do, dv_in, dv2 are fp16 (else bf16)
 constexpr int kBwdStateBF16 = 2;   // dht, dh0 are bf16 (else fp32)
 
+struct FusedArgs {
+    CUtensorMap tm_q, tm_k, tm_v;  // user inputs, 3-D {dim, H, rows}
+    const float* g;                // fp32 [rows, H, K]
+    const uint16_t* beta;          // bf16 bits [rows, H]
+    const float* h0;               // fp32 [N, H, K, V] or null
+    float* ht;                     // fp32 [N, H, K, V] or null
+    uint16_t* o;                   // bf16 bits [rows, H, V]
+    uint8_t* ws;                   // status word and sequence table (the planner's)
+    WsLayout L;
+    float scale;
+    int N, H, K, V;
+};
+
 cudaError_t launch_plan(const int32_t* cu_seqlens, int N, int B, int T, uint8_t* ws,
                         const WsLayout& L, cudaStream_t stream);
 cudaError_t launch_intra(const IntraArgs& a, cudaStream_t stream);
@@ -77,6 +90,9 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 // memory beyond their own need, so no intra-chunk CTA shares an SM with them.
 cudaError_t launch_scan_stage(const ScanArgs& a, int stage, cudaStream_t stream);
 cudaError_t launch_bwd_dh(const BwdArgs& a, cudaStream_t stream);
+// The single-pass forward: one CTA per (sequence, head), intra-chunk stage and
+// scan chunk by chunk on chip (bf16 I/O, fp32 state, activated beta).
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream);
 // Argument checks of the scan stage of kda_fwd (h0, o, ht, dims, workspace),
 // with no driver call and no launch: lets an entry point that runs the two
 // stages itself report every argument error before it enqueues anything.

@@ -125,6 +125,7 @@ bool map3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, i
 }
 
 bool check_opts(const kda_fwd_opts* op, const kda_dims* d) {
+    if (op->plan != KDA_PLAN_AUTO && op->plan != KDA_PLAN_TWO_STAGE && op->plan != KDA_PLAN_FUSED) return false;
     if (op->io_dtype != KDA_IO_BF16 && op->io_dtype != KDA_IO_F16) return false;
     if (op->state_dtype != KDA_STATE_F32 && op->state_dtype != KDA_STATE_BF16) return false;
     if (op->beta_logits != 0 && op->beta_logits != 1) return false;
@@ -523,11 +524,41 @@ kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* 
     // every argument of both stages is checked before any driver call or launch
     kda_status st = scan_check(h0, o, ht, dims, opts, workspace, workspace_bytes);
     if (st != KDA_OK) return st;
+    kda_fwd_opts op{};
+    if (opts) op = *opts;
+    // the single-pass kernel runs on request only (it leaves no intermediates in
+    // the workspace for kda_bwd_dh) and takes the default interface only
+    const bool fused = op.plan == KDA_PLAN_FUSED;
+    if (fused && (op.io_dtype != KDA_IO_BF16 || op.state_dtype != KDA_STATE_F32 || op.beta_logits != 0 ||
+                  (op.qk_heads != 0 && op.qk_heads != dims->H)))
+        return KDA_ERR_UNSUPPORTED;
     IntraArgs ia;
     bool run = false;
     st = intra_setup(q, k, v, g, beta, dims ? dims->H : 0, 0, cu_seqlens, dims, opts, workspace,
                                 workspace_bytes, &ia, &run);
     if (st != KDA_OK) return st;
+    if (fused) {
+        FusedArgs fa{};
+        fa.tm_q = ia.tm_q;
+        fa.tm_k = ia.tm_k;
+        fa.tm_v = ia.tm_v;
+        fa.g = g;
+        fa.beta = static_cast<const uint16_t*>(beta);
+        fa.h0 = static_cast<const float*>(h0);
+        fa.ht = static_cast<float*>(ht);
+        fa.o = static_cast<uint16_t*>(o);
+        fa.ws = ia.ws;
+        fa.L = ia.L;
+        fa.scale = scale;
+        fa.N = is_varlen(dims) ? dims->num_seqs : dims->B;
+        fa.H = dims->H;
+        fa.K = dims->K;
+        fa.V = dims->V;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        st = plan(cu_seqlens, dims, ia, s);
+        if (st != KDA_OK) return st;
+        return launch_fused(fa, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     ScanArgs sa;
     st = scan_setup(scale, h0, o, ht, dims, opts, workspace, workspace_bytes, &sa);
     if (st != KDA_OK) return st;

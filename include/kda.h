@@ -145,6 +145,20 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
  *                and value head h reads q / k head h / (dims->H / qk_heads)
  *                (grouped value heads, the "HV" heads of fwd_state.py).  q and
  *                k are then [B, T, qk_heads, K].
+ *   plan         KDA_PLAN_AUTO and KDA_PLAN_TWO_STAGE: the intra-chunk kernel
+ *                over every chunk, then the scan (segmented or staged as
+ *                kda_workspace_layout reports), leaving the intermediates in
+ *                the workspace for kda_bwd_dh.  KDA_PLAN_FUSED: the single-pass
+ *                kernel, one CTA per (sequence, head) running the intra-chunk
+ *                stage and the scan chunk by chunk on chip, so only q, k, v, g,
+ *                beta, h0 are read and o, ht written; the workspace then holds
+ *                only the status word and the tables (no intermediates: a
+ *                kda_bwd_dh needs a two-stage forward).  It takes the default
+ *                interface only (bf16 I/O, fp32 state, activated beta, equal
+ *                heads); other options with it return KDA_ERR_UNSUPPORTED.  A
+ *                sequence's chunks run one after another on one SM, so it is
+ *                slower than the two stages wherever those fill the GPU.
+ *                kda_fwd_intra_ex / kda_fwd_scan_ex ignore it.
  * The ABI types: h0 / ht pointers are `const void*` / `void*` here because
  * their element type follows state_dtype.  Invalid option values return
  * KDA_ERR_INVALID_ARG.
@@ -153,11 +167,15 @@ kda_status kda_fwd_scan(float scale, const float* h0, void* o, float* ht, const 
 #define KDA_IO_F16 1
 #define KDA_STATE_F32 0
 #define KDA_STATE_BF16 1
+#define KDA_PLAN_AUTO 0
+#define KDA_PLAN_TWO_STAGE 1
+#define KDA_PLAN_FUSED 2
 typedef struct kda_fwd_opts {
     int32_t io_dtype;
     int32_t state_dtype;
     int32_t beta_logits;
     int32_t qk_heads;
+    int32_t plan;
 } kda_fwd_opts;
 
 kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g, const void* beta,

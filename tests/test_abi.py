@@ -325,3 +325,22 @@ def test_context_parallel_entries_validate_before_any_launch(lib):
     assert chain(pq=0) == 1 and chain(h_in=0) == 1                    # NULL pointers
     assert chain(pq=FAKE + 4) == 3 and chain(h0=FAKE + 4) == 3        # misaligned
     assert chain(N=0) == 0                                            # nothing to do
+
+
+def test_fused_plan_options_validate_before_any_launch(lib):
+    """The plan option: unknown values are rejected, the single-pass kernel with
+    an interface variant is unsupported, both before any driver call; the
+    automatic plan takes the two stages (on this machine it then fails at its
+    first driver call, KDA_ERR_CUDA)."""
+    P = ctypes.c_void_p
+    d = kda.make_dims(1, 128, 2, 128, 128)
+
+    def fwd_ex(**kw):
+        o = kda.FwdOpts(**kw)
+        return lib.kda_fwd_ex(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0.1, None, None, P(FAKE), None,
+                              ctypes.byref(d), ctypes.byref(o), P(FAKE), 1 << 40, None)
+
+    assert fwd_ex(plan=3) == 1 and fwd_ex(plan=-1) == 1
+    assert fwd_ex(plan=2, io_dtype=1) == 2 and fwd_ex(plan=2, beta_logits=1) == 2
+    assert fwd_ex(plan=2, state_dtype=1) == 2 and fwd_ex(plan=2, qk_heads=1) == 2
+    assert fwd_ex(plan=0, io_dtype=1) == 5 and fwd_ex(plan=1) == 5
