@@ -40,6 +40,7 @@
 //    each chunk.
 #include <cuda_bf16.h>
 
+#include "chunk_math.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -49,65 +50,7 @@ namespace {
 using namespace ptx;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 256;
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-__device__ __forceinline__ float bf_at(const uint8_t* p) { return bf_lo((uint32_t)(*(const uint16_t*)p)); }
-
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-// d += a * b, one m16n8k8 fragment pair, tf32 operands, fp32 accumulation
-__device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* b) {
-    const uint32_t ah[4] = {tf32_rna(a[0]), tf32_rna(a[1]), tf32_rna(a[2]), tf32_rna(a[3])};
-    const uint32_t bh[2] = {tf32_rna(b[0]), tf32_rna(b[1])};
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(ah[0]), "r"(ah[1]), "r"(ah[2]), "r"(ah[3]), "r"(bh[0]), "r"(bh[1]));
-}
-
-// fp32 64x64 matrix, rows of 64 floats with the 8-float column group XORed by
-// (row & 3): A^T in the strict upper triangle, T below (its diagonal blocks
-// whole once A's have been consumed).
-struct Mat64 {
-    float* p;
-    __device__ __forceinline__ float* at(int r, int c) const { return p + r * 64 + (c ^ ((r & 3) << 3)); }
-};
-
-// Exact gated sums over one 64-dim key block, for a chunk whose decay span is
-// too large for the factored MMA: qk = [q 8K | ... | k 8K] at the given
-// offsets (SW128), g2h its g2 as fp32 [64][64].
-__device__ __noinline__ void exact_sums_block(const uint8_t* qs, const uint8_t* ks, const float* g2h, int valid,
-                                              float* ea, float* eb) {
-    constexpr int kPairs = 64 * 64 / kThreads;
-    for (int n = 0; n < kPairs; ++n) {
-        const int e = threadIdx.x + kThreads * n, i = e >> 6, j = e & 63;
-        if (j <= i && i < valid) {
-            float a = ea[n], b = eb[n];
-            for (int d = 0; d < 64; ++d) {
-                const float qi = bf_at(qs + sw128_offset(i, d));
-                const float ki = bf_at(ks + sw128_offset(i, d));
-                const float kj = bf_at(ks + sw128_offset(j, d));
-                const float gate = ex2(g2h[i * 64 + d] - g2h[j * 64 + d]);
-                a = fmaf(qi * kj, gate, a);
-                b = fmaf(ki * kj, gate, b);
-            }
-            ea[n] = a;
-            eb[n] = b;
-        }
-    }
-}
+constexpr int kThreads = kChunkThreads;
 
 template <int KB, int VB>
 struct FusedSmem {
@@ -134,6 +77,7 @@ struct FusedSmem {
     static constexpr uint32_t QKV_TX = (2 * KB + VB) * 8192;
     static constexpr uint32_t TMEM_COLS = VB == 2 ? 512 : 256;  // intra 128 + ACC V + DH V
     static_assert(NSEG * K * 4 == 4096, "segment sums are 4 KB");
+    static_assert(KX(0) - QG(0) == 8192, "exact_sums_block reads k 8 KB after q");
 };
 
 struct FusedBars {
@@ -361,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float4(gv[rr][0], gv[rr][1], gv[rr][2], gv[rr][3]);
                 }
                 __syncthreads();
-                exact_sums_block(sm + S::QG(kb), sm + S::KX(kb), g2h, valid, ea, eb);
+                exact_sums_block<false>(sm + S::QG(kb), g2h, valid, ea, eb);  // k exp2(g2) slot = qg slot + 8 KB
                 __syncthreads();
             }
 #pragma unroll
@@ -462,93 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
 
         // ---- 4. T = (I + A)^-1 by 16x16 blocks (fp32), then T' = T diag(beta) --
-        if (tid < 64) {
-            const int I = tid >> 4, cc = tid & 15, b0 = 16 * I;
-            float acc[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) acc[rr] = (rr == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < 15; ++m) {
-                const float tm = acc[m];
-#pragma unroll
-                for (int r4 = ((m + 1) / 4) * 4; r4 < 16; r4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(PM.at(b0 + m, b0 + r4));
-                    if (r4 + 0 > m) acc[r4 + 0] = fmaf(-a.x, tm, acc[r4 + 0]);
-                    if (r4 + 1 > m) acc[r4 + 1] = fmaf(-a.y, tm, acc[r4 + 1]);
-                    if (r4 + 2 > m) acc[r4 + 2] = fmaf(-a.z, tm, acc[r4 + 2]);
-                    acc[r4 + 3] = fmaf(-a.w, tm, acc[r4 + 3]);
-                }
-            }
-            asm volatile("bar.sync 1, 64;" ::: "memory");
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) *PM.at(b0 + rr, b0 + cc) = acc[rr];
-        }
-        __syncthreads();
-        {
-            const int gq = lane >> 2, t = lane & 3;
-            float* xw = Xsm + warp * 128;
-#pragma unroll 1
-            for (int lev = 1; lev < 4; ++lev) {
-                for (int item = warp; item < 2 * (4 - lev); item += kThreads / 32) {
-                    const int J = item >> 1, nh = item & 1, I = J + lev;
-                    const int n0 = 16 * J + 8 * nh;
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int Kb = J; Kb < I; ++Kb) {
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const int kc = 16 * Kb + 8 * ks;
-                            const float a[4] = {*PM.at(kc + t, 16 * I + gq), *PM.at(kc + t, 16 * I + gq + 8),
-                                                *PM.at(kc + t + 4, 16 * I + gq), *PM.at(kc + t + 4, 16 * I + gq + 8)};
-                            const float b[2] = {*PM.at(kc + t, n0 + gq), *PM.at(kc + t + 4, n0 + gq)};
-                            mma_tf32(acc, a, b);
-                        }
-                    }
-                    xw[gq * 8 + 2 * t] = acc[0];
-                    xw[gq * 8 + 2 * t + 1] = acc[1];
-                    xw[(gq + 8) * 8 + 2 * t] = acc[2];
-                    xw[(gq + 8) * 8 + 2 * t + 1] = acc[3];
-                    __syncwarp();
-                    float dd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const int kc = 16 * I + 8 * ks;
-                        const float a[4] = {*PM.at(16 * I + gq, kc + t), *PM.at(16 * I + gq + 8, kc + t),
-                                            *PM.at(16 * I + gq, kc + t + 4), *PM.at(16 * I + gq + 8, kc + t + 4)};
-                        const float b[2] = {xw[(8 * ks + t) * 8 + gq], xw[(8 * ks + t + 4) * 8 + gq]};
-                        mma_tf32(dd, a, b);
-                    }
-                    *reinterpret_cast<float2*>(PM.at(16 * I + gq, n0 + 2 * t)) = make_float2(-dd[0], -dd[1]);
-                    *reinterpret_cast<float2*>(PM.at(16 * I + gq + 8, n0 + 2 * t)) = make_float2(-dd[2], -dd[3]);
-                    __syncwarp();
-                }
-                __syncthreads();
-            }
-        }
-        {
-            const int i = tid >> 2, j0 = (tid & 3) * 16;
-            uint4 x[2];
-#pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8) {
-                const int j = j0 + 8 * q8;
-                const float4 ta = *reinterpret_cast<const float4*>(PM.at(i, j));
-                const float4 tb = *reinterpret_cast<const float4*>(PM.at(i, j + 4));
-                const float4 ba = *reinterpret_cast<const float4*>(beta_s + j);
-                const float4 bb = *reinterpret_cast<const float4*>(beta_s + j + 4);
-                const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-                const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = j + e <= i ? tv[e] * bv[e] : 0.f;
-                x[q8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                   pack_bf16x2(y[6], y[7]));
-            }
-            __syncthreads();
-#pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8) {
-                const int j = j0 + 8 * q8;
-                *reinterpret_cast<uint4*>(sm + S::M + i * 128 + (((j >> 3) ^ (i & 7)) << 4)) = x[q8];
-            }
-        }
+        unit_lower_inverse(PM, Xsm, tid, warp, lane);
+        store_t_prime(PM, beta_s, sm + S::M, tid);
         // v rows past the end of the sequence -> 0 (inert in u)
         for (int e = tid; e < (64 - valid) * 8 * VB; e += kThreads) {
             const int rr = valid + e / (8 * VB), x = e % (8 * VB);

@@ -56,6 +56,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "chunk_math.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -65,93 +66,7 @@ namespace {
 using namespace ptx;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 256;
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-
-// Inputs q, k, v, beta are bf16 or (F16) fp16; everything computed on chip and
-// every intermediate written to the workspace is bf16.
-template <bool F16>
-__device__ __forceinline__ float in_lo(uint32_t w) {
-    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
-    else return bf_lo(w);
-}
-template <bool F16>
-__device__ __forceinline__ float in_hi(uint32_t w) {
-    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
-    else return bf_hi(w);
-}
-template <bool F16>
-__device__ __forceinline__ float in_at(const uint8_t* p) {
-    return in_lo<F16>((uint32_t)(*(const uint16_t*)p));
-}
-
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-__device__ __forceinline__ void mma_tf32_16x8x8(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-// d += a * b for one m16n8k8 fragment pair with tf32 operands (round to nearest)
-// and fp32 accumulation.  A hi/lo operand split (3xTF32, fp32-level products)
-// was measured to change no parity figure in the fourth digit: T' is rounded
-// to bf16 right after, so single tf32 products suffice.
-__device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* b) {
-    const uint32_t ah[4] = {tf32_rna(a[0]), tf32_rna(a[1]), tf32_rna(a[2]), tf32_rna(a[3])};
-    const uint32_t bh[2] = {tf32_rna(b[0]), tf32_rna(b[1])};
-    mma_tf32_16x8x8(d, ah, bh);
-}
-
-// fp32 64x64 matrix in shared memory, row-major with 64 floats per row and an
-// XOR of the column's 8-float group by (row & 3): row-contiguous accesses,
-// float4 row reads and the 4-row x 8-column fragment reads of the MMAs are
-// all free of bank conflicts.  It holds A^T in its strict upper triangle and
-// T in its strict lower triangle (T's diagonal 16x16 blocks whole, once A's
-// have been consumed).
-struct Mat64 {
-    float* p;
-    __device__ __forceinline__ float* at(int r, int c) const { return p + r * 64 + (c ^ ((r & 3) << 3)); }
-};
-
-// Exact gated sums of a chunk whose decay span is too large for the factored
-// MMA (kept out of line so its registers do not weigh on the common path),
-// accumulated over one 64-dim block of key dims: qk is the block's raw
-// [q 8K | k 8K] tiles (SW128), g2h its g2 as fp32 [64][64].  For this thread's
-// (i, j) pairs, ea += q_i . k_j gated (j <= i) and eb += k_i . k_j gated.
-template <bool F16>
-__device__ __noinline__ void exact_sums_block(const uint8_t* qk, const float* g2h, int valid, float* ea,
-                                              float* eb) {
-    constexpr int kPairs = 64 * 64 / kThreads;
-    for (int n = 0; n < kPairs; ++n) {
-        const int e = threadIdx.x + kThreads * n, i = e >> 6, j = e & 63;
-        if (j <= i && i < valid) {
-            float a = ea[n], b = eb[n];
-            for (int d = 0; d < 64; ++d) {
-                const float qi = in_at<F16>(qk + sw128_offset(i, d));
-                const float ki = in_at<F16>(qk + 8192 + sw128_offset(i, d));
-                const float kj = in_at<F16>(qk + 8192 + sw128_offset(j, d));
-                const float gate = ex2(g2h[i * 64 + d] - g2h[j * 64 + d]);
-                a = fmaf(qi * kj, gate, a);
-                b = fmaf(ki * kj, gate, b);
-            }
-            ea[n] = a;
-            eb[n] = b;
-        }
-    }
-}
+constexpr int kThreads = kChunkThreads;
 
 template <int KB, int VB>
 struct IntraSmem {
@@ -493,103 +408,10 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
     }
     __syncthreads();
-    // ---- 4. T = (I + A)^-1 by 16x16 blocks, fp32, into M's strict lower triangle
-    // level 0: diagonal blocks by forward substitution (column per thread)
-    if (tid < 64) {
-        const int I = tid >> 4, cc = tid & 15, b0 = 16 * I;
-        float acc[16];
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) acc[rr] = (rr == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 15; ++m) {
-            const float tm = acc[m];
-#pragma unroll
-            for (int r4 = ((m + 1) / 4) * 4; r4 < 16; r4 += 4) {
-                // A[b0 + r][b0 + m] for r = r4..r4+3: one float4 of A^T row b0 + m;
-                // only r > m is A (the rest is T's storage)
-                const float4 a = *reinterpret_cast<const float4*>(PM.at(b0 + m, b0 + r4));
-                if (r4 + 0 > m) acc[r4 + 0] = fmaf(-a.x, tm, acc[r4 + 0]);
-                if (r4 + 1 > m) acc[r4 + 1] = fmaf(-a.y, tm, acc[r4 + 1]);
-                if (r4 + 2 > m) acc[r4 + 2] = fmaf(-a.z, tm, acc[r4 + 2]);
-                acc[r4 + 3] = fmaf(-a.w, tm, acc[r4 + 3]);
-            }
-        }
-        // acc is column cc of T_II whole (1 on the diagonal, 0 above it); it
-        // replaces A's diagonal block once every column's substitution is done
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) *PM.at(b0 + rr, b0 + cc) = acc[rr];
-    }
-    __syncthreads();
-    // levels 1..3: T_IJ = -T_II * (sum_{J<=K<I} A_IK T_KJ), J = I - lev.  One warp per
-    // (block, 8-column half): 16x8 outputs by warp-level m16n8k8 tf32 MMAs.
-    {
-        const int gq = lane >> 2, t = lane & 3;
-        float* xw = Xsm + warp * 128;  // this warp's X half, [16][8] fp32
-#pragma unroll 1
-        for (int lev = 1; lev < 4; ++lev) {
-            for (int item = warp; item < 2 * (4 - lev); item += kThreads / 32) {
-                const int J = item >> 1, nh = item & 1, I = J + lev;
-                const int n0 = 16 * J + 8 * nh;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int Kb = J; Kb < I; ++Kb) {
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const int kc = 16 * Kb + 8 * ks;
-                        const float a[4] = {*PM.at(kc + t, 16 * I + gq), *PM.at(kc + t, 16 * I + gq + 8),
-                                            *PM.at(kc + t + 4, 16 * I + gq), *PM.at(kc + t + 4, 16 * I + gq + 8)};
-                        const float b[2] = {*PM.at(kc + t, n0 + gq), *PM.at(kc + t + 4, n0 + gq)};
-                        mma_tf32(acc, a, b);
-                    }
-                }
-                xw[gq * 8 + 2 * t] = acc[0];
-                xw[gq * 8 + 2 * t + 1] = acc[1];
-                xw[(gq + 8) * 8 + 2 * t] = acc[2];
-                xw[(gq + 8) * 8 + 2 * t + 1] = acc[3];
-                __syncwarp();
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int kc = 16 * I + 8 * ks;
-                    const float a[4] = {*PM.at(16 * I + gq, kc + t), *PM.at(16 * I + gq + 8, kc + t),
-                                        *PM.at(16 * I + gq, kc + t + 4), *PM.at(16 * I + gq + 8, kc + t + 4)};
-                    const float b[2] = {xw[(8 * ks + t) * 8 + gq], xw[(8 * ks + t + 4) * 8 + gq]};
-                    mma_tf32(d, a, b);
-                }
-                *reinterpret_cast<float2*>(PM.at(16 * I + gq, n0 + 2 * t)) = make_float2(-d[0], -d[1]);
-                *reinterpret_cast<float2*>(PM.at(16 * I + gq + 8, n0 + 2 * t)) = make_float2(-d[2], -d[3]);
-                __syncwarp();
-            }
-            __syncthreads();
-        }
-    }
-    // T' = T diag(beta) -> bf16, K-major SW128 [64 i][64 j], written over M once
-    // every thread has read its part of T
-    {
-        const int i = tid >> 2, j0 = (tid & 3) * 16;
-        uint4 x[2];
-#pragma unroll
-        for (int q8 = 0; q8 < 2; ++q8) {
-            const int j = j0 + 8 * q8;
-            const float4 ta = *reinterpret_cast<const float4*>(PM.at(i, j));
-            const float4 tb = *reinterpret_cast<const float4*>(PM.at(i, j + 4));
-            const float4 ba = *reinterpret_cast<const float4*>(beta_s + j);
-            const float4 bb = *reinterpret_cast<const float4*>(beta_s + j + 4);
-            const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-            const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = j + e <= i ? tv[e] * bv[e] : 0.f;
-            x[q8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                               pack_bf16x2(y[6], y[7]));
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q8 = 0; q8 < 2; ++q8) {
-            const int j = j0 + 8 * q8;
-            *reinterpret_cast<uint4*>(sm + S::M + i * 128 + (((j >> 3) ^ (i & 7)) << 4)) = x[q8];
-        }
-    }
+    // ---- 4. T = (I + A)^-1 by 16x16 blocks, fp32, into M's strict lower
+    // triangle; then T' = T diag(beta) in bf16 over M
+    unit_lower_inverse(PM, Xsm, tid, warp, lane);
+    store_t_prime(PM, beta_s, sm + S::M, tid);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();

@@ -34,6 +34,7 @@
 // roles unwind without trapping.
 #include <cuda_bf16.h>
 
+#include "chunk_math.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -42,13 +43,6 @@ namespace {
 
 using namespace ptx;
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
