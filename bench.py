@@ -72,7 +72,7 @@ def flops_per_token_head(K, V, C=64):
 
 
 # headers every kernel translation unit compiles in (PTX wrappers, layouts)
-KERNEL_HEADERS = ("ptx.cuh", "common.cuh", "internal.h")
+KERNEL_HEADERS = ("ptx.cuh", "common.cuh", "internal.h", "chunk_math.cuh")
 
 
 def source_sha(path):
@@ -554,7 +554,8 @@ def run_gb300(args):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
-                     "launch_ms_statistic": "median over the split steps"},
+                     "launch_ms_statistic": ("median of the timed steps (planner launch included)" if fused
+                                             else "median over the split steps")},
         "step_roofline": step_roofline(K, V, th, hstate, ms_per_step, hbm, tc),
         "kernels_ms": {"intra": intra_med, "scan": scan_med, "note": "medians of separate split steps with an "
                        "event between the kernels over every chunk; the timed steps run them back to back"
