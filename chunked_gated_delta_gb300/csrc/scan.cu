@@ -66,13 +66,26 @@ struct ScanCfg {
     static constexpr uint32_t TMEM_COLS = NVB == 1 ? 256 : 512;
     // the one-stage variant runs two CTAs per SM (registers capped at 128)
     static constexpr int MIN_CTAS = (NVB == 1 && STAGES == 1) ? 2 : 1;
-    // one input stage
-    static constexpr uint32_t AW = 0;                    // per kb: [w 8K | qg 8K]
-    static constexpr uint32_t AQK = AW + 2 * KB * 8192;  // Aqk [64][64]; the 8K before it = rows 64..
-    static constexpr uint32_t KG = AQK + 8192;           // kg per kb [64 tok][64 d]
-    static constexpr uint32_t U = KG + KB * 8192;        // u per V block [64 tok][64 v]
-    static constexpr uint32_t STAGE = U + NVB * 8192;
-    static constexpr uint32_t TX_BYTES = (3 * KB + 1 + NVB) * 8192 + K * 4;
+    // One input stage, in two parts: part A holds what the u and WH MMAs read
+    // (and gd), part B what DH and the output MMAs read.  In the 128-column
+    // shape (SPLIT) each part has its own barriers, so part A of a later chunk
+    // starts loading as soon as WH has read this one, about half a chunk
+    // before DH and the output are done.  The 64-column shapes keep one
+    // barrier phase per chunk: each phase of TMA loads costs an SM about as
+    // much as 7 KB of data (measured on GB300), more than the earlier start
+    // of a 40 KB part A gains there.
+    static constexpr bool SPLIT = NVB == 2;
+    static constexpr uint32_t AW = 0;  // part A: per kb [w 8K | qg 8K]
+    // split: [AW | u | kg | Aqk]; one phase: [AW | Aqk | kg | u] (the order
+    // measured fastest for each)
+    static constexpr uint32_t U = SPLIT ? AW + 2 * KB * 8192 : AW + (3 * KB + 1) * 8192;  // u per V block
+    static constexpr uint32_t KG = SPLIT ? U + NVB * 8192 : AW + (2 * KB + 1) * 8192;     // part B: kg per kb
+    static constexpr uint32_t AQK = SPLIT ? KG + KB * 8192 : AW + 2 * KB * 8192;          // Aqk [64][64]
+    // the 8K before Aqk (kg, or qg in the one-phase order) are the unused A
+    // rows 0..63 of the output MMA
+    static constexpr uint32_t STAGE = AW + (3 * KB + 1 + NVB) * 8192;
+    static constexpr uint32_t TXA_BYTES = (2 * KB + NVB) * 8192 + K * 4;
+    static constexpr uint32_t TXB_BYTES = (KB + 1) * 8192;
     // persistent
     static constexpr uint32_t HS = STAGES * STAGE;       // h bf16 per V block [K rows][64 v], MN-major SW128
     static constexpr uint32_t HS_BLOCK = KB * 8192;
@@ -91,7 +104,7 @@ struct ScanCfg {
 
 template <int STAGES>
 struct ScanBars {
-    uint64_t full[STAGES], empty[STAGES];
+    uint64_t full_a[STAGES], empty_a[STAGES], full_b[STAGES], empty_b[STAGES];
     uint64_t h_ready, wh_full, vp_ready, dh_full;
     uint64_t acc_full[2], acc_empty[2];
     uint32_t tmem_slot;
@@ -148,8 +161,10 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&B.full[i], 1);
-            mbar_init(&B.empty[i], 1 + S::REC_WARPS);
+            mbar_init(&B.full_a[i], 1);
+            mbar_init(&B.empty_a[i], 1 + S::REC_WARPS);
+            mbar_init(&B.full_b[i], 1);
+            mbar_init(&B.empty_b[i], 1);
         }
         mbar_init(&B.h_ready, S::REC_WARPS);
         mbar_init(&B.wh_full, 1);
@@ -274,8 +289,13 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
         for (int it = 0; it < nit && !*abort_flag; ++it) {
             const int st = it % STAGES;
             const uint32_t sp = (it / STAGES) & 1;
-            uint8_t* stage = sm + st * S::STAGE;
-            if (!wait(&B.full[st], sp)) break;
+            if (!wait(&B.full_a[st], sp)) break;
+            // gd is the only part of the stage these warps read
+            const float decay = has_row ? ex2(reinterpret_cast<const float*>(sm + S::GDS + st * K * 4)[r]) : 0.f;
+            if (S::SPLIT) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.empty_a[st]);
+            }
             if (quad < 2) {
                 // v'[r, :] = u[r, :] - WH[r, :]
                 // v'[r, :] = u[r, :] - WH[r, :], formed in TMEM by the MMAs
@@ -301,7 +321,6 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.vp_ready);
             }
-            const float decay = has_row ? ex2(reinterpret_cast<const float*>(sm + S::GDS + st * K * 4)[r]) : 0.f;
             if (!wait(&B.dh_full, it & 1)) break;
             tc_fence_after();
             if (has_row) {
@@ -315,8 +334,10 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 }
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.empty[st]);
+            if (!S::SPLIT) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.empty_a[st]);
+            }
             write_h();
         }
         if (map_mode && has_row && !timed_out && !*abort_flag) {
@@ -357,30 +378,31 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             prefetch_tmap(&tm_aqk);
             const float* gd = reinterpret_cast<const float*>(ws + L.gd);
             // map mode reads neither qg nor Aqk (no output) nor u for P columns
-            uint32_t tx = S::TX_BYTES;
+            uint32_t txa = S::TXA_BYTES, txb = S::TXB_BYTES;
             if (map_mode) {
-                tx -= (KB + 1) * 8192;
+                txa -= KB * 8192;  // no qg
+                txb -= 8192;       // no Aqk
 #pragma unroll
                 for (int vb = 0; vb < NVB; ++vb)
-                    if (v0 + vb * 64 < K) tx -= 8192;
+                    if (v0 + vb * 64 < K) txa -= 8192;
             }
             for (int it = 0; it < nit && !*abort_flag; ++it) {
                 const int c = c_begin + it;
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
-                if (!wait(&B.empty[st], sp ^ 1)) break;
+                if (!wait(&B.empty_a[st], sp ^ 1)) break;
                 uint8_t* stage = sm + st * S::STAGE;
                 const int64_t tile = (int64_t)(si.tile_base + c) * H + h;
                 const int row = (int)(tile * 64);
-                uint64_t* fb = &B.full[st];
-                mbar_arrive_expect_tx(fb, tx);
+                uint64_t* fb = &B.full_a[st];
+                mbar_arrive_expect_tx(fb, S::SPLIT ? txa : txa + txb);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb) {
                     tma_load_2d(stage + S::AW + kb * 16384, &tm_w, fb, kb * 64, row);
                     if (!map_mode) tma_load_2d(stage + S::AW + kb * 16384 + 8192, &tm_qg, fb, kb * 64, row);
-                    tma_load_2d(stage + S::KG + kb * 8192, &tm_kg, fb, kb * 64, row);
+                    if (!S::SPLIT) tma_load_2d(stage + S::KG + kb * 8192, &tm_kg, fb, kb * 64, row);
                 }
-                if (!map_mode) tma_load_2d(stage + S::AQK, &tm_aqk, fb, 0, row);
+                if (!S::SPLIT && !map_mode) tma_load_2d(stage + S::AQK, &tm_aqk, fb, 0, row);
 #pragma unroll
                 for (int vb = 0; vb < NVB; ++vb) {
                     const int cb = v0 + vb * 64;
@@ -388,6 +410,14 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                     else if (cb >= K) tma_load_2d(stage + S::U + vb * 8192, &tm_u, fb, cb - K, row);
                 }
                 bulk_load_1d(sm + S::GDS + st * K * 4, gd + tile * K, K * 4, fb);
+                if (S::SPLIT) {
+                    if (!wait(&B.empty_b[st], sp ^ 1)) break;
+                    fb = &B.full_b[st];
+                    mbar_arrive_expect_tx(fb, txb);
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) tma_load_2d(stage + S::KG + kb * 8192, &tm_kg, fb, kb * 64, row);
+                    if (!map_mode) tma_load_2d(stage + S::AQK, &tm_aqk, fb, 0, row);
+                }
             }
         }
     } else if (warp == S::MMA_WARP) {
@@ -396,45 +426,52 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
             constexpr uint32_t id_h = idesc_bf16_f32(128, S::BV, 0, 1);   // A K-major, B (u, h, v') MN-major
             constexpr uint32_t id_hn = idesc_bf16_f32(128, S::BV, 0, 1, 1);  // the same with A negated
             constexpr uint32_t id_dh = idesc_bf16_f32(128, S::BV, 1, 1);  // A = kg^T MN-major
+            // operand descriptors built once (the ring's at stage 0); the issue
+            // loop steps them by constant offsets and the stage
+            const uint64_t d_idn = smem_desc(sbase + S::IDN, 16, 1024);
+            const uint64_t d_hs = smem_desc(sbase + S::HS, S::HS_BLOCK, 1024);
+            const uint64_t d_vp = smem_desc(sbase + S::VP, 8192, 1024);
+            const uint64_t d_u = smem_desc(sbase + S::U, 8192, 1024);
+            const uint64_t d_aw = smem_desc(sbase + S::AW, 16, 1024);
+            const uint64_t d_kg = smem_desc(sbase + S::KG, 8192, 1024);
+            const uint64_t d_aqk = smem_desc(sbase + S::AQK - 8192, 16, 1024);
             for (int it = 0; it < nit && !*abort_flag; ++it) {
                 const int st = it % STAGES;
                 const uint32_t sp = (it / STAGES) & 1;
                 const int buf = it & 1;
                 const uint32_t bp = (it >> 1) & 1;
-                const uint32_t stage = sbase + st * S::STAGE;
-                if (!wait(&B.full[st], sp)) break;
+                const uint32_t so = (uint32_t)st * S::STAGE;  // this stage's offset in the ring
+                if (!wait(&B.full_a[st], sp)) break;
                 if (!wait(&B.acc_empty[buf], bp ^ 1)) break;
                 tc_fence_after();
                 const uint32_t d_acc = t_acc + buf * S::BV;
                 // ACC = [I ; 0] @ u, ahead of the state
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(d_acc, smem_desc(sbase + S::IDN + ks * 32, 16, 1024),
-                             smem_desc(stage + S::U + ks * 2048, 8192, 1024), id_h, ks > 0 ? 1u : 0u);
+                    mma_bf16(d_acc, desc_at(d_idn, ks * 32), desc_at(d_u, so + ks * 2048), id_h, ks > 0 ? 1u : 0u);
                 if (!wait(&B.h_ready, it & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < K / 16; ++ks) {
                     const int kb = ks >> 2, kk = ks & 3;
-                    mma_bf16(d_acc, smem_desc(stage + S::AW + kb * 16384 + kk * 32, 16, 1024),
-                             smem_desc(sbase + S::HS + ks * 2048, S::HS_BLOCK, 1024), id_hn, 1u);
+                    mma_bf16(d_acc, desc_at(d_aw, so + kb * 16384 + kk * 32), desc_at(d_hs, ks * 2048), id_hn, 1u);
                 }
                 mma_commit(&B.wh_full);
+                if (S::SPLIT) mma_commit(&B.empty_a[st]);  // u and WH have read part A
                 if (!wait(&B.vp_ready, it & 1)) break;
+                if (S::SPLIT && !wait(&B.full_b[st], sp)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(t_dh, smem_desc(stage + S::KG + ks * 2048, 8192, 1024),
-                             smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_dh, ks > 0 ? 1u : 0u);
+                    mma_bf16(t_dh, desc_at(d_kg, so + ks * 2048), desc_at(d_vp, ks * 2048), id_dh, ks > 0 ? 1u : 0u);
                 mma_commit(&B.dh_full);
                 if (!map_mode) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(d_acc, smem_desc(stage + S::AQK - 8192 + ks * 32, 16, 1024),
-                                 smem_desc(sbase + S::VP + ks * 2048, 8192, 1024), id_hn, 1u);
+                        mma_bf16(d_acc, desc_at(d_aqk, so + ks * 32), desc_at(d_vp, ks * 2048), id_hn, 1u);
                 }
                 mma_commit(&B.acc_full[buf]);
-                mma_commit(&B.empty[st]);
+                mma_commit(S::SPLIT ? &B.empty_b[st] : &B.empty_a[st]);
             }
         }
     } else {
