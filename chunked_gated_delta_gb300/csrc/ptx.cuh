@@ -236,12 +236,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
-// The descriptor of an operand `bytes` past the one that `d` describes, with
-// the same strides: the offset (16-byte aligned) goes into the 14-bit start
-// address field, which cannot carry since shared memory ends below 256 KB.
-// Issue loops build each operand's descriptor once and step it with this.
-__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
-
 // Instruction descriptor, .kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand is MN-major (1) or K-major (0); neg_a: D (+)= (-A) B.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn, int neg_a = 0) {

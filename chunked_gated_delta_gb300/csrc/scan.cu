@@ -44,6 +44,12 @@ namespace {
 using namespace ptx;
 
 
+// The descriptor of an operand `bytes` past the one that `d` describes, with
+// the same strides: the offset (16-byte aligned) goes into the 14-bit start
+// address field, which cannot carry since shared memory ends below 256 KB.
+// The issue loop builds each operand's descriptor once and steps it with this.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
