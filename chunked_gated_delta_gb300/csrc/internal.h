@@ -9,6 +9,27 @@
 
 namespace kda {
 
+// Launches kern after the previous kernel in stream with programmatic stream
+// serialization: its CTAs may become resident while that kernel's last CTAs
+// run, and each of them calls grid_dep_wait() before it reads anything the
+// earlier kernels wrote.  Used only where the previous work in the stream is
+// the kernel whose results this one reads (no event waits in between).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct IntraArgs {
     CUtensorMap tm_q, tm_k, tm_v;            // user inputs, 3-D {dim, H, rows}
     CUtensorMap st_qg, st_w, st_u;           // workspace tiles (stores), 2-D {dim, tiles*64}
@@ -23,6 +44,7 @@ struct IntraArgs {
     int f16;                             // q, k, v, beta are fp16 (else bf16)
     int flags;                           // kIntraBetaLogits
     int group;                           // value heads per q/k head
+    int after_planner;                   // launched right after the planner in the same stream (PDL)
 };
 
 constexpr int kIntraBetaLogits = 1;

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kThreads, 4)
     __shared__ uint64_t bar_qk, bar_v, bar_mma;
     __shared__ uint32_t tmem_slot;
 
+    // launched after the planner: its chunk table and status word first
+    grid_dep_launch();
+    grid_dep_wait();
     const int64_t tile = blockIdx.x;  // chunk * H + head
     const int c = static_cast<int>(tile / H), h = static_cast<int>(tile % H);
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
@@ -532,6 +535,10 @@ cudaError_t launch_intra_t(const IntraArgs& a, cudaStream_t stream) {
     // -> 0.434 ms at the headline; half an SM-count or less, and 4 x SMs, ran
     // slower than none); at K = 64 every distance tried ran slower, so off
     const int pf_dist = KB == 2 ? 5 * device_sm_count() / 4 : 0;
+    if (a.after_planner)
+        return launch_dependent(kern, dim3((unsigned)ctas), dim3(kThreads), smem, stream, a.tm_q, a.tm_k, a.tm_v,
+                                a.st_qg, a.st_w, a.st_u, a.g, a.beta, a.ws, a.L, a.H, a.flags, a.group,
+                                a.beta_stride, a.beta_head0, pf_dist);
     kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.st_qg, a.st_w, a.st_u, a.g,
                                                      a.beta, a.ws, a.L, a.H, a.flags, a.group, a.beta_stride,
                                                      a.beta_head0, pf_dist);

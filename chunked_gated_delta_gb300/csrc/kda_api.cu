@@ -255,6 +255,7 @@ kda_status intra_setup(const void* q, const void* k, const void* v, const float*
     a->group = dims->H / hqk;
     a->beta_stride = beta_stride;
     a->beta_head0 = beta_head0;
+    a->after_planner = 1;  // every caller launches the planner, then this kernel, on one stream
     return KDA_OK;
 }
 
@@ -396,6 +397,7 @@ kda_status run_stages(const IntraArgs& ia, const ScanArgs& sa, cudaStream_t s) {
         const int64_t c0 = (int64_t)j * L.stage_len;
         const int64_t c1 = std::min<int64_t>(c0 + L.stage_len, L.max_chunks);
         IntraArgs aj = ia;
+        aj.after_planner = 0;  // follows event waits on the library's intra stream
         aj.max_chunks = c1 - c0;
         aj.L.chunk_info += (size_t)c0 * sizeof(ChunkInfo);
         aj.L.gd += (size_t)(c0 * H) * ia.K * sizeof(float);

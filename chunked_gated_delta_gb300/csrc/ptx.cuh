@@ -114,6 +114,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
         "l"(m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may become resident before the previous kernel in its stream
+// has finished.  grid_dep_wait() blocks until that kernel has completed and
+// its writes are visible (at once if there is none); grid_dep_launch() lets
+// this kernel's own dependents start launching once every CTA of it has run it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // L2 prefetches (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m), "r"(c0), "r"(c1),

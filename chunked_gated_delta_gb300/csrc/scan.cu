@@ -150,6 +150,10 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
     const int s = blockIdx.x / (NT * H);
     const int seg = seg_base + (int)blockIdx.y;
     const int v0 = vt * S::BV;
+    // launched after the kernel whose results this one reads (the intra
+    // kernel, the map pass or the combine step)
+    grid_dep_launch();
+    grid_dep_wait();
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
     const SeqInfo si = reinterpret_cast<const SeqInfo*>(ws + L.seq_info)[s];
@@ -590,8 +594,11 @@ cudaError_t launch_scan_t(const ScanArgs& a, int mode, cudaStream_t stream, int 
         flags |= kScanExitToHin;
     }
     const dim3 grid((unsigned)ctas, (unsigned)segs);
+    if (stage < 0)  // the staged forward's ranges follow event waits: plain launches there
+        return launch_dependent(kern, grid, dim3(S::THREADS), smem, stream, a.tm_w, a.tm_qg, a.tm_kg, a.tm_u,
+                                a.tm_aqk, a.tm_o, a.h0, a.ht, a.o, a.ws, L, a.scale, a.N, a.H, a.V, flags, mode, 0);
     kern<<<grid, S::THREADS, smem, stream>>>(a.tm_w, a.tm_qg, a.tm_kg, a.tm_u, a.tm_aqk, a.tm_o, a.h0, a.ht, a.o, a.ws,
-                                             L, a.scale, a.N, a.H, a.V, flags, mode, stage >= 0 ? stage : 0);
+                                             L, a.scale, a.N, a.H, a.V, flags, mode, stage);
     return cudaGetLastError();
 }
 
@@ -650,6 +657,8 @@ __global__ void __launch_bounds__(2 * K) kda_seg_combine_kernel(const void* __re
     float4* Hs = csm4 + 2 * K * K4;  // 2 x [K][C / 4]
     const int NTV = V / C;
     const int vt = blockIdx.x % NTV, h = (blockIdx.x / NTV) % H, s = blockIdx.x / (NTV * H);
+    grid_dep_launch();
+    grid_dep_wait();  // the map pass (or the caller's earlier work) has written pq
     if (status != nullptr && *reinterpret_cast<const volatile int32_t*>(status) != 0) return;
     int nseg = nseg_fixed;
     if (nseg_fixed <= 0) {
@@ -761,8 +770,8 @@ cudaError_t launch_combine_raw(const void* h0, const float* pq, float* hin, cons
     if (e != cudaSuccess) return e;
     const int64_t ctas = (int64_t)N * H * (V / kCombineCols);
     if (ctas <= 0) return cudaSuccess;
-    kern<<<(unsigned)ctas, 2 * K, smem, stream>>>(h0, pq, hin, status, seqs, seg_len, nseg_fixed, N, H, V, flags);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)ctas), dim3(2 * K), smem, stream, h0, pq, hin, status, seqs, seg_len,
+                            nseg_fixed, N, H, V, flags);
 }
 
 template <int K>
