@@ -11,9 +11,10 @@ namespace kda {
 
 // Launches kern after the previous kernel in stream with programmatic stream
 // serialization: its CTAs may become resident while that kernel's last CTAs
-// run, and each of them calls grid_dep_wait() before it reads anything the
-// earlier kernels wrote.  Used only where the previous work in the stream is
-// the kernel whose results this one reads (no event waits in between).
+// run.  Every kernel launched this way calls grid_dep_wait() before it reads
+// or writes global memory, so it is correct after any earlier work; the
+// staged forward's launches, which follow event waits on the library's
+// streams, stay plain launches all the same.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                     cudaStream_t stream, Args... args) {

@@ -78,8 +78,8 @@ struct ScanCfg {
     // starts loading as soon as WH has read this one, about half a chunk
     // before DH and the output are done.  The 64-column shapes keep one
     // barrier phase per chunk: each phase of TMA loads costs an SM about as
-    // much as 7 KB of data (measured on GB300), more than the earlier start
-    // of a 40 KB part A gains there.
+    // much as seven 8 KB boxes of data (measured on GB300), more than the
+    // earlier start of a 40 KB part A gains there.
     static constexpr bool SPLIT = NVB == 2;
     static constexpr uint32_t AW = 0;  // part A: per kb [w 8K | qg 8K]
     // split: [AW | u | kg | Aqk]; one phase: [AW | Aqk | kg | u] (the order
@@ -307,7 +307,6 @@ __global__ void __launch_bounds__(ScanCfg<KB, NVB, STAGES>::THREADS, ScanCfg<KB,
                 if (lane == 0) mbar_arrive(&B.empty_a[st]);
             }
             if (quad < 2) {
-                // v'[r, :] = u[r, :] - WH[r, :]
                 // v'[r, :] = u[r, :] - WH[r, :], formed in TMEM by the MMAs
                 if (!wait(&B.wh_full, it & 1)) break;
                 tc_fence_after();
