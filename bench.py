@@ -75,12 +75,39 @@ def flops_per_token_head(K, V, C=64):
 KERNEL_HEADERS = ("ptx.cuh", "common.cuh", "internal.h", "chunk_math.cuh")
 
 
+def code_text(src):
+    """C / CUDA source without its comments and blank lines (string and
+    character literals kept as written), so that a change to comments alone
+    leaves a kernel's key unchanged and any change to code changes it."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        ch = src[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and src[j] != ch:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_sha(path):
-    """sha256 prefix of a kernel source together with the headers it includes."""
+    """sha256 prefix of a kernel source together with the headers it includes,
+    over their code (comments and blank lines left out)."""
     h = hashlib.sha256()
     for p in [path] + [os.path.join(os.path.dirname(path), n) for n in KERNEL_HEADERS]:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -100,3 +100,26 @@ def test_percentiles_and_strict_roofline():
     r = bench.step_roofline(128, 128, 1000, 0, 1.0, 1000.0, 1000.0)
     assert r["bytes"] == 3858 * 1000 and r["strict_io_bytes"] == 1538 * 1000
     assert abs(r["frac_of_strict_io_bound"] - 1538e3 / 1e12 * 1e3) < 1e-12
+
+
+def test_kernel_key_ignores_comments_only(tmp_path):
+    """The key that ties a committed ncu traffic figure to a kernel source
+    changes with the code and not with its comments or blank lines."""
+    src = ('// header\n#include "h.cuh"\n/* block\n   comment */\n__global__ void k(int* p) {\n'
+           '    const char* s = "a // b /* c */";  // trailing\n    char q = \'\\\'\';\n\n    p[0] = 1;\n}\n')
+    headers = {n: "// only a comment\nint x_%d;\n" % i for i, n in enumerate(bench.KERNEL_HEADERS)}
+
+    def key(text):
+        d = tmp_path / str(abs(hash(text)))
+        d.mkdir()
+        for n, body in headers.items():
+            (d / n).write_text(body)
+        (d / "k.cu").write_text(text)
+        return bench.source_sha(str(d / "k.cu"))
+
+    base = key(src)
+    assert key(src.replace("// trailing", "// another remark").replace("// header", "")) == base
+    assert key(src.replace("\n\n", "\n\n\n")) == base
+    assert key(src.replace("p[0] = 1;", "p[0] = 2;")) != base
+    assert key(src.replace('"a // b /* c */"', '"a // b"')) != base  # literals are code
+    assert "// b /* c */" in bench.code_text(src) and "trailing" not in bench.code_text(src)
