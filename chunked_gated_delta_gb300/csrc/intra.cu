@@ -474,14 +474,16 @@ __global__ void __launch_bounds__(kThreads, 4)
     // ---- 6. w^T / u^T -> swizzled [i][dim] staging -> TMA stores -------------
     // Each warp reads 16-lane (dim) x 32-column (token) blocks in the m16n8
     // fragment layout and writes them transposed, 8x8 bf16 matrices at a time.
+    // w first: its stores read their staging while the warps stage u, so the
+    // tile's end waits only for u's.
     {
         const int quad = warp & 3, i0 = (warp >> 2) * 32;  // TMEM lane quadrant, token-row half
         const int mat = lane >> 3, mrow = lane & 7;         // the stmatrix row this lane addresses
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int L0 = quad * 32 + half * 16;  // dims L0 .. L0 + 15
+        for (int wu = 0; wu < 2; ++wu) {        // 0: w (columns i0..), 1: u (columns 64 + i0..)
 #pragma unroll
-            for (int wu = 0; wu < 2; ++wu) {        // 0: w (columns i0..), 1: u (columns 64 + i0..)
+            for (int half = 0; half < 2; ++half) {
+                const int L0 = quad * 32 + half * 16;  // dims L0 .. L0 + 15
                 if (L0 >= (wu == 0 ? K : V)) continue;
                 uint32_t r[16];
                 tmem_ld16x256_x4(tmem + ((uint32_t)L0 << 16) + wu * 64 + i0, r);
@@ -498,19 +500,22 @@ __global__ void __launch_bounds__(kThreads, 4)
                                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
                 }
             }
+            fence_proxy_async_smem();
+            if (wu == 1) tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                if (wu == 0) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb) tma_store_2d(&st_w, sm + S::QK + kb * 16384, kb * 64, trow);
+                } else {
+#pragma unroll
+                    for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::ustg(vb), vb * 64, trow);
+                }
+                bulk_commit();
+            }
         }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb) tma_store_2d(&st_w, sm + S::QK + kb * 16384, kb * 64, trow);
-#pragma unroll
-        for (int vb = 0; vb < VB; ++vb) tma_store_2d(&st_u, sm + S::ustg(vb), vb * 64, trow);
-        bulk_commit();
-        bulk_wait_read0();  // smem must outlive the reads; the writes complete with the grid
-    }
+    if (tid == 0) bulk_wait_read0();  // smem must outlive the reads; the writes complete with the grid
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
